@@ -1,0 +1,75 @@
+"""Quest page metadata and page criticality bound, fp64.
+
+Source: "Quest 完全拆解：查询感知的页级稀疏注意力" (pinghaoyang.com.cn),
+sections 核心机制 (the per-dimension bound U_i = max(q_i m_i, q_i M_i) and
+its two-case proof) and 关键性估计算法 (incremental M_i <- max(M_i, k_i),
+m_i <- min(m_i, k_i) on insert; score = sum_i max(q_i M_i, q_i m_i) at
+attention time).  GQA handling follows the same page's "GQA 下的并集放大"
+section: one selection shared by the query heads of a kv-head group; the
+group score is the largest per-head bound, so the bound still holds for
+every query head of the group.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def page_token_range(p: int, page_size: int, seq_len: int) -> tuple[int, int]:
+    """Logical token range [t0, t1) of page p that holds valid tokens."""
+    t0 = p * page_size
+    return t0, min(t0 + page_size, seq_len)
+
+
+def num_pages(seq_len: int, page_size: int) -> int:
+    return -(-seq_len // page_size)
+
+
+def page_minmax(k_pool, page_table, seq_lens, page_size):
+    """Per-channel min m and max M of K over the valid tokens of each page.
+
+    k_pool: [P_phys][Hkv][S][d] (any real dtype; values are exact in fp64).
+    Returns an fp64 array [P_phys][Hkv][2][d] (index 0 = m, 1 = M) with NaN
+    in pages that no sequence uses.
+    """
+    k_pool = np.asarray(k_pool)
+    P_phys, Hkv, S, d = k_pool.shape
+    out = np.full((P_phys, Hkv, 2, d), np.nan)
+    for b, L in enumerate(seq_lens):
+        for p in range(num_pages(int(L), page_size)):
+            phys = int(page_table[b][p])
+            t0, t1 = page_token_range(p, page_size, int(L))
+            keys = k_pool[phys, :, : t1 - t0, :].astype(np.float64)  # [Hkv][n][d]
+            out[phys, :, 0, :] = keys.min(axis=1)
+            out[phys, :, 1, :] = keys.max(axis=1)
+    return out
+
+
+def minmax_append(meta_page, k_new, slot):
+    """Incremental update of one page's (m, M) on inserting key k_new.
+
+    meta_page: fp64 [2][d] (m, M); slot: the token's index inside its page.
+    The first token of a page starts the page's statistics.
+    """
+    k_new = np.asarray(k_new, dtype=np.float64)
+    if slot == 0:
+        return np.stack([k_new.copy(), k_new.copy()])
+    return np.stack([np.minimum(meta_page[0], k_new), np.maximum(meta_page[1], k_new)])
+
+
+def head_bound(q_head, m, M):
+    """sum_i max(q_i m_i, q_i M_i) for one query head over pages.
+
+    q_head: [d]; m, M: [P][d].  Returns [P] fp64.
+    """
+    q = np.asarray(q_head, dtype=np.float64)[None, :]
+    return np.sum(np.maximum(q * m, q * M), axis=-1)
+
+
+def group_scores(q_group, m, M):
+    """Page score for a kv-head group: the largest per-head bound.
+
+    q_group: [G][d] query rows of the group; m, M: [P][d].  Returns [P].
+    """
+    per_head = np.stack([head_bound(qh, m, M) for qh in np.asarray(q_group, dtype=np.float64)])
+    return per_head.max(axis=0)
