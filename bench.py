@@ -1,0 +1,530 @@
+"""Decode-step benchmark of query-aware sparse-page attention on GB300.
+
+One step = the whole hot path over one batch: page-metadata update for the
+token just appended, page scoring, exact top-k, split-K sparse flash-decoding
+and the log-sum-exp combine, on one "layer" of KV cache.  Layers rotate over
+R independent cache replicas so that no step is served from L2 (the bytes a
+step touches times R exceed four times the L2 size).
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores instead, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from synth import get_workload, make_inputs  # noqa: E402
+
+METRIC = "decode attn steps/s and effective HBM GB/s (% of 8 TB/s) vs dense at 32K–128K"
+DEFAULT_WORKLOAD = "llama2-7b-mha-32k"
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------- utils
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+        }
+
+
+# ------------------------------------------------------------------- byte model
+def step_bytes(w, lens, sel_tokens, cand_pages, sel_pages):
+    """Algorithmic HBM bytes of one select + attend step (metadata of every
+    scored page, K/V (+ scales) of every attended token, q, out + lse, page ids)."""
+    kvb = 1 if w.kv_dtype == "i8" else 2
+    scale = 2 if w.kv_dtype == "i8" else 0
+    if w.selector == "quest":
+        meta = cand_pages * 2 * w.head_dim * kvb
+    else:
+        meta = cand_pages * (w.page_size * w.sketch_dim // 2 + 4)
+    kv = sel_tokens * 2 * (w.head_dim * kvb + scale)
+    q = w.batch * w.num_q_heads * w.head_dim * 2
+    out = w.batch * w.num_q_heads * (w.head_dim + 1) * 4
+    return meta, kv, q + out + sel_pages * 8
+
+
+def selection_stats(w, inp, sel, sel_cnt):
+    """Attended tokens, scored candidate pages and selected pages, summed over units."""
+    S = w.page_size
+    lens = inp.seq_lens.cpu().tolist()
+    cnt = sel_cnt.cpu().numpy()
+    sel_h = sel.cpu().numpy()
+    sel_tok = cand = sel_pages = 0
+    for b, L in enumerate(lens):
+        P = -(-L // S)
+        lo = min(w.n_sink, P)
+        hi = max(P - w.n_recent, lo)
+        cand += (hi - lo) * w.num_kv_heads
+        for h in range(w.num_kv_heads):
+            n = int(cnt[b, h])
+            sel_pages += n
+            # every page is full except the sequence's last one
+            last_in = n > 0 and int(sel_h[b, h, n - 1]) == P - 1
+            sel_tok += n * S - (P * S - L if last_in else 0)
+    return sel_tok, cand, sel_pages
+
+
+# ----------------------------------------------------------------- our GPU arm
+def run_ours(args, world, rank, local):
+    import torch.distributed as dist
+
+    import query_aware_sparse_page_gb300 as spg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = get_workload(args.workload)
+    R = args.layers
+    layers = []
+    for layer in range(R):
+        inp = make_inputs(w, device=dev, seed_offset=1000 * rank + layer)
+        p = spg.params_for(inp)
+        bufs = spg.alloc_buffers(p, dev)
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 1,
+                                    bufs.minmax, bufs.sketch, bufs.sketch_scale, inp.proj, bufs.ws)
+        layers.append((inp, p, bufs))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        inp, p, b = layers[i % R]
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 0,
+                                    b.minmax, b.sketch, b.sketch_scale, inp.proj, b.ws)
+        spg.sparse_decode_select_attend(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                        inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                                        b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.out, b.lse,
+                                        b.ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def timed(fn, K):
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms / K
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        step(i)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_step = timed(step, K)
+    clock_info = clocks.stop()
+
+    # per-kernel attribution: the same step split into its entry points, events between
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        inp, p, b = layers[i % R]
+        ev[i][0].record(stream)
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 0,
+                                    b.minmax, b.sketch, b.sketch_scale, inp.proj, b.ws)
+        ev[i][1].record(stream)
+        spg.sparse_page_select(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                               b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.ws)
+        ev[i][2].record(stream)
+        spg.sparse_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                    inp.page_table, inp.seq_lens, b.sel, b.sel_cnt, b.out, b.lse,
+                                    b.ws)
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    ph = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(3)] for i in range(K)]).mean(0)
+    # the select phase alone on its score kernel (one launch per call)
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    e_s[0].record(stream)
+    for i in range(K):
+        inp, p, b = layers[i % R]
+        spg.sparse_page_score(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                              b.sketch_scale, inp.proj, b.scores, b.ws)
+        e_s[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms_score = float(np.mean([e_s[i].elapsed_time(e_s[i + 1]) for i in range(K)]))
+
+    # dense baseline over the same caches
+    def dense(i):
+        inp, p, b = layers[i % R]
+        spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                   inp.page_table, inp.seq_lens, b.out, b.lse, b.ws)
+
+    for i in range(W):
+        dense(i)
+    ms_dense = timed(dense, K)
+
+    # bytes
+    inp0, p0, b0 = layers[0]
+    sel_tok, cand, sel_pages = selection_stats(w, inp0, b0.sel, b0.sel_cnt)
+    meta_b, kv_b, small_b = step_bytes(w, None, sel_tok, cand, sel_pages)
+    total_b = meta_b + kv_b + small_b
+    lens = inp0.seq_lens.cpu().tolist()
+    dense_tok = sum(lens) * w.num_kv_heads
+    kvb = 1 if w.kv_dtype == "i8" else 2
+    dense_b = dense_tok * 2 * (w.head_dim * kvb + (2 if w.kv_dtype == "i8" else 0)) + small_b
+    peak, peak_kind = measured_peaks()
+
+    # roofline of the dominant phase
+    phases = {"meta_update": ph[0], "select(score+topk)": ph[1], "attention(attn+combine)": ph[2]}
+    dom = max(phases, key=phases.get)
+    if dom.startswith("attention"):
+        dom_bytes, dom_ms, kname = kv_b + small_b, ph[2], "k_attn+k_combine"
+    elif dom.startswith("select"):
+        dom_bytes, dom_ms, kname = meta_b, ms_score, "k_quest_score" if w.selector == "quest" else "k_sketch_score"
+    else:
+        dom_bytes, dom_ms, kname = 0, ph[0], "meta"
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else 0.0
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, spg, layers, stream, world, dev)
+
+    steps_s = world * 1000.0 / ms_step
+    gbs = world * total_b / (ms_step * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(steps_s, 2),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "kv_dtype": w.kv_dtype,
+        "data": "synthetic (seeded; shapes and distributions of the workload recipe)",
+        "config": {
+            "workload": w.name,
+            "batch": w.batch, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "page_size": w.page_size, "seq_len": w.seq_len or list(w.seq_range),
+            "token_budget": w.token_budget, "selector": w.selector,
+            "layers_rotated": R,
+            "l2": f"inputs larger than L2: {R} rotating cache replicas, each step reads "
+                  f"{total_b / 1e6:.1f} MB of a distinct replica",
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "hbm_gbs_effective": round(gbs, 1),
+        "hbm_frac_nominal": round(gbs / world / NOMINAL_HBM_GBS, 4),
+        "hbm_frac_measured": round(gbs / world / peak, 4),
+        "bytes_per_step": {"metadata": meta_b, "selected_kv": kv_b, "q_out_idx": small_b, "total": total_b},
+        "dense": {
+            "steps_per_s": round(world * 1000.0 / ms_dense, 2),
+            "ms_per_step": round(ms_dense, 5),
+            "bytes_per_step": dense_b,
+            "hbm_gbs": round(dense_b / (ms_dense * 1e-3) / 1e9, 1),
+            "speedup_sparse_vs_dense": round(ms_dense / ms_step, 3),
+        },
+        "phase_ms": {k: round(float(v), 5) for k, v in phases.items()},
+        "roofline": {
+            "kernel": kname,
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_kind": peak_kind,
+            "traffic": None,
+            "algorithmic_bytes": dom_bytes,
+            "ms_per_launch": round(float(dom_ms), 5),
+        },
+        "clocks": clock_info,
+        "e2e": e2e,
+        "gpu_launches": K * (5 if w.selector != "all" else 2),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, layers[0][0], budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def run_e2e(args, spg, layers, stream, world, dev):
+    """Same step through the public API with host buffers: q and the appended
+    token's K/V go host -> device each step, out and lse come back."""
+    K = max(5, args.steps // 2)
+    R = len(layers)
+    hosts = []
+    for inp, p, b in layers:
+        w = inp.workload
+        q_h = inp.q.cpu().pin_memory()
+        lens = inp.seq_lens.cpu().tolist()
+        kv_rows = []
+        for bb, L in enumerate(lens):
+            if L <= 0:
+                continue
+            t = L - 1
+            phys = int(inp.page_table[bb, t // w.page_size])
+            k_h = inp.k_pool[phys, :, t % w.page_size].cpu().pin_memory()
+            v_h = inp.v_pool[phys, :, t % w.page_size].cpu().pin_memory()
+            kv_rows.append((phys, t % w.page_size, k_h, v_h))
+        out_h = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+        lse_h = torch.empty(b.lse.shape, dtype=b.lse.dtype).pin_memory()
+        hosts.append((q_h, kv_rows, out_h, lse_h))
+    h2d = d2h = 0
+
+    def e2e_step(i):
+        nonlocal h2d, d2h
+        inp, p, b = layers[i % R]
+        q_h, kv_rows, out_h, lse_h = hosts[i % R]
+        inp.q.copy_(q_h, non_blocking=True)
+        h2d_i = q_h.numel() * q_h.element_size()
+        for phys, slot, k_h, v_h in kv_rows:
+            inp.k_pool[phys, :, slot].copy_(k_h, non_blocking=True)
+            inp.v_pool[phys, :, slot].copy_(v_h, non_blocking=True)
+            h2d_i += 2 * k_h.numel() * k_h.element_size()
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 0,
+                                    b.minmax, b.sketch, b.sketch_scale, inp.proj, b.ws)
+        spg.sparse_decode_select_attend(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                        inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                                        b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.out, b.lse,
+                                        b.ws)
+        out_h.copy_(b.out, non_blocking=True)
+        lse_h.copy_(b.lse, non_blocking=True)
+        stream.synchronize()  # the host reads the result every step
+        h2d, d2h = h2d_i, out_h.numel() * 4 + lse_h.numel() * 4
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        e2e_step(i)
+    dt = (time.perf_counter() - t0) / K
+    return {"value": round(world / dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_unit_inputs(inp, b, h):
+    from oracle import decode
+
+    w = inp.workload
+    S, G = w.page_size, w.group
+    L = int(inp.seq_lens[b])
+    P = -(-L // S)
+    phys = inp.page_table[b, :P].long()
+
+    def npy(t):
+        if t is None:
+            return None
+        t = t[phys][:, h : h + 1].cpu()
+        return (t.float() if t.dtype == torch.bfloat16 else t).numpy()
+
+    q = inp.q[b : b + 1, h * G : (h + 1) * G].cpu()
+    q = (q.float() if q.dtype == torch.bfloat16 else q).numpy()
+    proj = None if inp.proj is None else inp.proj.cpu().numpy()
+    return decode.StepInputs(q, npy(inp.k_pool), npy(inp.v_pool), npy(inp.k_scale), npy(inp.v_scale),
+                             np.arange(max(P, 1))[None, :], np.array([L]), proj)
+
+
+def cpu_baseline(w, inp, budget_s=12.0, max_units=None):
+    """Time the oracle, as it stands, on (batch, kv-head) units of one step."""
+    from oracle import decode
+
+    prm = decode.StepParams(w.page_size, w.n_sel_pages, w.n_sink, w.n_recent, w.selector, w.head_dim)
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    if max_units:
+        units = units[:max_units]
+    done, t_total = 0, 0.0
+    for b, h in units:
+        sub = _oracle_unit_inputs(inp, b, h)
+        t0 = time.perf_counter()
+        decode.decode_step(sub, prm, units=[(0, 0)])
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    step_s = t_total * len(units) / done
+    return {"value": round(1.0 / step_s, 6), "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {len(units)} (batch, kv-head) units of one step of {w.name}, "
+                      f"{t_total:.1f} s of fp64 numpy on one host core, scaled to a whole step"}
+
+
+def run_reference(args, world, rank, local):
+    """The oracle as the reference arm: rank 0 only, host cores."""
+    if rank != 0:
+        return
+    w = get_workload(args.workload)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(w, device=dev)
+    K, W = args.steps, args.warmup
+    per_step = max(0.2, min(1.0, 120.0 / max(K + W, 1)))
+    n_units = w.batch * w.num_kv_heads
+    from oracle import decode
+
+    prm = decode.StepParams(w.page_size, w.n_sel_pages, w.n_sink, w.n_recent, w.selector, w.head_dim)
+    subs = {}
+
+    def one_step(i):
+        # a bounded sample of the step: as many units as fit in the per-step budget
+        t0 = time.perf_counter()
+        done = 0
+        while done < n_units:
+            u = (i * 7 + done) % n_units
+            b, h = divmod(u, w.num_kv_heads)
+            if (b, h) not in subs:
+                subs[(b, h)] = _oracle_unit_inputs(inp, b, h)
+            decode.decode_step(subs[(b, h)], prm, units=[(0, 0)])
+            done += 1
+            if time.perf_counter() - t0 >= per_step:
+                break
+        return (time.perf_counter() - t0) * n_units / done, done
+
+    for i in range(W):
+        one_step(i)
+    times, units = [], 0
+    for i in range(K):
+        t, d = one_step(i)
+        times.append(t)
+        units += d
+    step_s = float(np.mean(times))
+    val = 1.0 / step_s
+    res = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(val, 6),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(step_s * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; shapes and distributions of the workload recipe)",
+        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "page_size": w.page_size, "seq_len": w.seq_len or list(w.seq_range),
+                   "token_budget": w.token_budget, "selector": w.selector},
+        "cpu_baseline": {"value": round(val, 6), "unit": "steps/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{units} (batch, kv-head) units over {K} timed steps of "
+                                   f"{n_units}; each step scaled from its sampled units"},
+        "e2e": {"value": round(val, 6), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, local)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+/*
+ * spg.h — C ABI of the query-aware sparse-page decode attention library
+ * (libspg.so, hand-written CUDA for sm_103a).
+ *
+ * One decode step over a paged KV cache:
+ *   1. keep per-page metadata current when a token is appended
+ *      (Quest 完全拆解, 关键性估计算法: M_i <- max(M_i, k_i), m_i <- min(m_i, k_i);
+ *       SALS长序列推理优化, 算法简介: the low-rank index-key preprocessing),
+ *   2. score every candidate page against the current query
+ *      (Quest 核心机制: sum_i max(q_i m_i, q_i M_i);  SALS Quant Sals Indexer:
+ *       int4 low-rank index key, dequantise, block log-sum-exp),
+ *   3. take the exact top-k pages, lower page index winning ties, plus forced
+ *      sink / recent (tail) pages (SALS QSI Top-k 计算实现; Day 10·2 sparse top-k
+ *      块选择, 确定性红线), writing only int32 page ids (SequenceO1 close
+ *      reading §3.3, the select -> attend two-kernel boundary),
+ *   4. run split-K flash-decoding over the selected pages only and merge the
+ *      splits by log-sum-exp (SALS SFAA 四阶段 flow; AICPU Tiling challenge 2).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers, 16-byte aligned, contiguous
+ *     row-major in the layouts stated below; the caller owns all memory.
+ *     The library never allocates device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise, except spg_read_device_error.
+ *   - Nothing throws across the ABI.  Host-side checks return SPG_EINVAL
+ *     (bad sizes, null or misaligned pointers), SPG_EUNSUPPORTED (valid but
+ *     not built: e.g. head_dim outside {64, 128}), SPG_EWORKSPACE (workspace
+ *     too small) before anything is launched; a failed launch is SPG_ECUDA.
+ *   - Faults the device can see (a page-table entry outside the pool, a
+ *     seq_len beyond the page table, a selected page id out of range, a
+ *     bounded wait that ran out) are not dereferenced: the offending page is
+ *     skipped and a bit (SPG_DEVERR_*) is OR-ed into the error word at the
+ *     start of the workspace.  spg_read_device_error() fetches it.
+ *   - The workspace must be zero-filled once after allocation; the library
+ *     leaves its bookkeeping in a reusable state after every call.
+ *
+ * Shapes (B batch, Hq / Hkv query / kv heads, G = Hq / Hkv, d head_dim,
+ * S page_size, P_phys num_phys_pages, MP max_pages_per_seq,
+ * n_sel = token_budget / page_size, ds sketch_dim):
+ *   q            [B][Hq][d]            q_dtype (fp16 | bf16); query head j
+ *                                      belongs to kv-head j / G
+ *   k_pool,v_pool[P_phys][Hkv][S][d]   kv_dtype (fp16 | bf16 | int8)
+ *   k_scale,v_scale [P_phys][Hkv][S]   fp16, per-token per-head dequant
+ *                                      scales (int8 pools only, else NULL)
+ *   page_table   [B][MP] int32         physical page of each logical page
+ *   seq_lens     [B] int32             tokens in each sequence, counting the
+ *                                      token appended this step
+ *   minmax       [P_phys][Hkv][2][d]   kv_dtype; [..][0][:] = per-channel
+ *                                      min m, [..][1][:] = max M of K over
+ *                                      the page's valid tokens (Quest)
+ *   sketch       [P_phys][Hkv][S][ds/2] uint8; int4 codes of the projected
+ *                                      keys, two's complement, channel 2j in
+ *                                      the low nibble of byte j (sketch)
+ *   sketch_scale [P_phys][Hkv] fp32    one dequant scale per block (sketch)
+ *   proj         [d][ds] fp32          fixed projection P shared by all heads
+ *   scores       [B][Hkv][MP] fp32     page scores; -inf for pages that are
+ *                                      not candidates
+ *   sel          [B][Hkv][n_sel] int32 selected logical page ids, ascending;
+ *                                      unused tail entries are -1
+ *   sel_cnt      [B][Hkv] int32        number of valid entries in sel
+ *   out          [B][Hq][d] fp32       attention output
+ *   lse          [B][Hq] fp32          natural-log log-sum-exp of the scaled
+ *                                      logits over the attended tokens
+ *                                      (may be NULL)
+ * A sequence with seq_len 0 gets out = 0 and lse = -inf.
+ */
+#ifndef SPG_H_
+#define SPG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* spg_stream_t; /* a cudaStream_t */
+
+#define SPG_ABI_VERSION 1
+
+typedef enum {
+  SPG_OK = 0,
+  SPG_EINVAL = 1,
+  SPG_EUNSUPPORTED = 2,
+  SPG_ECUDA = 3,
+  SPG_EWORKSPACE = 4
+} spg_status;
+
+typedef enum {
+  SPG_SEL_QUEST = 0,       /* per-page per-channel min/max upper bound */
+  SPG_SEL_SKETCH_INT4 = 1, /* int4 low-rank index key, block log-sum-exp */
+  SPG_SEL_ALL = 2          /* every page (dense attention) */
+} spg_selector;
+
+typedef enum { SPG_F16 = 0, SPG_BF16 = 1, SPG_I8 = 2 } spg_dtype;
+
+/* device error bits, OR-ed into the workspace error word */
+#define SPG_DEVERR_PAGE_ID 1 /* page-table entry outside [0, num_phys_pages) */
+#define SPG_DEVERR_SEQ_LEN 2 /* seq_lens[b] < 0 or > max_pages_per_seq * page_size */
+#define SPG_DEVERR_SEL 4     /* sel entry outside [0, P_b) or sel_cnt outside [0, n_sel] */
+#define SPG_DEVERR_TIMEOUT 8 /* a bounded wait for an asynchronous copy ran out */
+
+typedef struct spg_params {
+  int32_t batch;             /* B >= 1 */
+  int32_t num_q_heads;       /* Hq, a multiple of num_kv_heads, G = Hq/Hkv in {1,2,4,8} */
+  int32_t num_kv_heads;      /* Hkv >= 1 */
+  int32_t head_dim;          /* d in {64, 128} */
+  int32_t page_size;         /* S: 8, 16, 32, 64 or 128 tokens (a SALS block) */
+  int32_t num_phys_pages;    /* P_phys: pages in the pool */
+  int32_t max_pages_per_seq; /* MP: columns of page_table */
+  int32_t kv_dtype;          /* spg_dtype */
+  int32_t q_dtype;           /* SPG_F16 or SPG_BF16; equal to kv_dtype unless kv is int8 */
+  int32_t selector;          /* spg_selector */
+  int32_t token_budget;      /* tokens attended per (batch, kv-head), forced pages
+                                included; a multiple of page_size; ignored by SPG_SEL_ALL */
+  int32_t n_sink_pages;      /* pages [0, n_sink) always attended */
+  int32_t n_recent_pages;    /* last n_recent pages always attended; the sketch
+                                selector needs >= 1 (the open tail block) */
+  int32_t sketch_dim;        /* ds = 16 for SPG_SEL_SKETCH_INT4, else ignored */
+  float softmax_scale;       /* 0 => 1/sqrt(head_dim) */
+} spg_params;
+
+/* Library ABI version (SPG_ABI_VERSION of the build). */
+int32_t spg_abi_version(void);
+
+/* Static text for a status code. */
+const char* spg_status_str(int32_t status);
+
+/* Host-only check of a parameter block: SPG_OK, SPG_EINVAL or SPG_EUNSUPPORTED. */
+spg_status spg_validate(const spg_params* p);
+
+/* Bytes of device workspace every entry point needs for these parameters
+ * (the same figure for all of them).  Host only. */
+spg_status spg_workspace_size(const spg_params* p, size_t* bytes);
+
+/* Metadata maintenance (Quest 关键性估计算法, insert-time update; SALS low-rank
+ * preprocessing).
+ * rebuild == 0 (append): for each sequence the token at position
+ *   seq_lens[b]-1 has just been written to the pools.  Quest: its page's
+ *   min/max is updated (the page's first token starts them afresh).
+ *   Sketch: when that token completes a block, the block's S keys are
+ *   dequantised, projected through proj and quantised to int4 with one scale.
+ * rebuild != 0: the metadata of every page of every sequence is rebuilt from
+ *   the pool (Quest: every page; sketch: every full block).
+ * Quest needs minmax (sketch args may be NULL); the sketch selector needs
+ * sketch, sketch_scale and proj (minmax may be NULL); k_scale for int8. */
+spg_status sparse_page_meta_update(const spg_params* p, const void* k_pool, const void* k_scale,
+                                   const int32_t* page_table, const int32_t* seq_lens,
+                                   int32_t rebuild, void* minmax, uint8_t* sketch,
+                                   float* sketch_scale, const float* proj, void* ws,
+                                   size_t ws_bytes, spg_stream_t stream);
+
+/* Page scores of every candidate page (Quest 核心机制; SALS QSI steps 1-3).
+ * Candidates of sequence b are pages [n_sink, P_b - n_recent); every other
+ * entry of the [B][Hkv][MP] array is -inf.  Quest: the largest over the
+ * group's query heads of sum_i max(q_i m_i, q_i M_i).  Sketch: with the
+ * group-mean query projected and quantised to int8 codes qc (scale sq),
+ * z_t = (sum_j qc_j kc_tj) * sq * sk_block / sqrt(d) and the block score is
+ * log sum_t exp(z_t). */
+spg_status sparse_page_score(const spg_params* p, const void* q, const int32_t* page_table,
+                             const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
+                             const float* sketch_scale, const float* proj, float* scores, void* ws,
+                             size_t ws_bytes, spg_stream_t stream);
+
+/* Score + exact top-k (SALS QSI steps 1-5; Quest Top-K filtering).  Per
+ * (batch, kv-head): forced pages F = [0, n_sink) U [P_b - n_recent, P_b);
+ * the k_top = n_sel - |F| best candidates by (score desc, page asc); sel =
+ * F U top-k in ascending order, sel_cnt = its size (all pages when
+ * P_b <= n_sel). */
+spg_status sparse_page_select(const spg_params* p, const void* q, const int32_t* page_table,
+                              const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
+                              const float* sketch_scale, const float* proj, int32_t* sel,
+                              int32_t* sel_cnt, void* ws, size_t ws_bytes, spg_stream_t stream);
+
+/* Flash-decoding over the selected pages only (SALS SFAA; Quest
+ * Approximate attention): for query head j of kv-head h, attention over
+ * the tokens t < seq_lens[b] of pages sel[b][h][0..sel_cnt), softmax
+ * renormalised over them (Day 10·2: the softmax covers the selected blocks
+ * only).  int8 K/V are dequantised by their per-token scales. */
+spg_status sparse_decode_attention(const spg_params* p, const void* q, const void* k_pool,
+                                   const void* v_pool, const void* k_scale, const void* v_scale,
+                                   const int32_t* page_table, const int32_t* seq_lens,
+                                   const int32_t* sel, const int32_t* sel_cnt, float* out,
+                                   float* lse, void* ws, size_t ws_bytes, spg_stream_t stream);
+
+/* sparse_page_select followed by sparse_decode_attention, one call. */
+spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const void* k_pool,
+                                       const void* v_pool, const void* k_scale,
+                                       const void* v_scale, const int32_t* page_table,
+                                       const int32_t* seq_lens, const void* minmax,
+                                       const uint8_t* sketch, const float* sketch_scale,
+                                       const float* proj, int32_t* sel, int32_t* sel_cnt,
+                                       float* out, float* lse, void* ws, size_t ws_bytes,
+                                       spg_stream_t stream);
+
+/* Dense flash-decoding over every page of every sequence (the baseline the
+ * Quest page compares against: the full KV read). */
+spg_status dense_decode_attention(const spg_params* p, const void* q, const void* k_pool,
+                                  const void* v_pool, const void* k_scale, const void* v_scale,
+                                  const int32_t* page_table, const int32_t* seq_lens, float* out,
+                                  float* lse, void* ws, size_t ws_bytes, spg_stream_t stream);
+
+/* Waits for `stream`, then copies the workspace error word to *bits. */
+spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t stream);
+
+/* Clears the workspace error word (asynchronous on `stream`). */
+spg_status spg_clear_device_error(void* ws, spg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPG_H_ */

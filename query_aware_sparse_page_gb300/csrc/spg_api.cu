@@ -1,0 +1,276 @@
+// C ABI of libspg: parameter validation, workspace layout, launch sequencing.
+// Everything here runs on the host; all device work is in the kernel files.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "spg_common.cuh"
+#include "spg_internal.h"
+
+namespace spg {
+
+int n_sel_pages(const spg_params& p) { return p.token_budget / p.page_size; }
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t workspace_bytes(const spg_params& p) {
+  const size_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads, d = p.head_dim;
+  const size_t MP = p.max_pages_per_seq;
+  size_t off = 256;                                      // header: error word
+  off += align256(sizeof(float) * B * Hkv * MP);         // scores
+  off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pm
+  off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pl
+  off += align256(sizeof(float) * B * Hq * kMaxSplits * d);  // pacc
+  return off;
+}
+
+Workspace carve_workspace(const spg_params& p, void* ws) {
+  const size_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads, d = p.head_dim;
+  const size_t MP = p.max_pages_per_seq;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  Workspace w{};
+  w.err = reinterpret_cast<int32_t*>(base);
+  size_t off = 256;
+  w.scores = reinterpret_cast<float*>(base + off);
+  off += align256(sizeof(float) * B * Hkv * MP);
+  w.pm = reinterpret_cast<float*>(base + off);
+  off += align256(sizeof(float) * B * Hq * kMaxSplits);
+  w.pl = reinterpret_cast<float*>(base + off);
+  off += align256(sizeof(float) * B * Hq * kMaxSplits);
+  w.pacc = reinterpret_cast<float*>(base + off);
+  return w;
+}
+
+}  // namespace spg
+
+using spg::Workspace;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+spg_status check_ws(const spg_params* p, const void* ws, size_t ws_bytes) {
+  if (!ok_ptr(ws)) return SPG_EINVAL;
+  if (ws_bytes < spg::workspace_bytes(*p)) return SPG_EWORKSPACE;
+  return SPG_OK;
+}
+
+spg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SPG_OK : SPG_ECUDA; }
+
+// the selector's metadata inputs
+spg_status check_meta_inputs(const spg_params* p, const void* minmax, const uint8_t* sketch,
+                             const float* sketch_scale, const float* proj) {
+  if (p->selector == SPG_SEL_QUEST) return ok_ptr(minmax) ? SPG_OK : SPG_EINVAL;
+  if (p->selector == SPG_SEL_SKETCH_INT4)
+    return (ok_ptr(sketch) && ok_ptr(sketch_scale) && ok_ptr(proj)) ? SPG_OK : SPG_EINVAL;
+  return SPG_EINVAL;  // SPG_SEL_ALL has no metadata and no selection
+}
+
+spg_status check_kv(const spg_params* p, const void* k_pool, const void* v_pool,
+                    const void* k_scale, const void* v_scale) {
+  if (!ok_ptr(k_pool) || !ok_ptr(v_pool)) return SPG_EINVAL;
+  if (p->kv_dtype == SPG_I8 && (!ok_ptr(k_scale) || !ok_ptr(v_scale))) return SPG_EINVAL;
+  return SPG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t spg_abi_version(void) { return SPG_ABI_VERSION; }
+
+const char* spg_status_str(int32_t s) {
+  switch (s) {
+    case SPG_OK: return "ok";
+    case SPG_EINVAL: return "invalid argument";
+    case SPG_EUNSUPPORTED: return "unsupported configuration";
+    case SPG_ECUDA: return "CUDA launch error";
+    case SPG_EWORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+spg_status spg_validate(const spg_params* p) {
+  if (!p) return SPG_EINVAL;
+  if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return SPG_EINVAL;
+  if (p->num_q_heads % p->num_kv_heads) return SPG_EINVAL;
+  if (p->head_dim < 32 || p->head_dim % 32) return SPG_EINVAL;
+  if (p->page_size < 8 || p->page_size > 128 || (p->page_size & (p->page_size - 1)))
+    return SPG_EINVAL;
+  if (p->num_phys_pages < 1 || p->max_pages_per_seq < 1) return SPG_EINVAL;
+  if (static_cast<int64_t>(p->max_pages_per_seq) * p->page_size > INT32_MAX) return SPG_EINVAL;
+  if (p->kv_dtype < SPG_F16 || p->kv_dtype > SPG_I8) return SPG_EINVAL;
+  if (p->q_dtype != SPG_F16 && p->q_dtype != SPG_BF16) return SPG_EINVAL;
+  if (p->kv_dtype != SPG_I8 && p->q_dtype != p->kv_dtype) return SPG_EINVAL;
+  if (p->selector < SPG_SEL_QUEST || p->selector > SPG_SEL_ALL) return SPG_EINVAL;
+  if (!(p->softmax_scale >= 0.f) || std::isinf(p->softmax_scale)) return SPG_EINVAL;
+  if (p->selector != SPG_SEL_ALL) {
+    if (p->n_sink_pages < 0 || p->n_recent_pages < 0) return SPG_EINVAL;
+    if (p->token_budget < p->page_size || p->token_budget % p->page_size) return SPG_EINVAL;
+    if (spg::n_sel_pages(*p) < p->n_sink_pages + p->n_recent_pages) return SPG_EINVAL;
+  }
+  if (p->selector == SPG_SEL_SKETCH_INT4) {
+    if (p->sketch_dim != 16) return SPG_EINVAL;
+    if (p->n_recent_pages < 1) return SPG_EINVAL;  // the open tail block is never scored
+  }
+  // valid, but not built
+  const int G = p->num_q_heads / p->num_kv_heads;
+  if (p->head_dim != 64 && p->head_dim != 128) return SPG_EUNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return SPG_EUNSUPPORTED;
+  if (p->selector == SPG_SEL_QUEST && p->kv_dtype == SPG_I8) return SPG_EUNSUPPORTED;
+  if (p->selector != SPG_SEL_ALL && p->max_pages_per_seq > spg::kMaxTopkPages)
+    return SPG_EUNSUPPORTED;
+  if (p->max_pages_per_seq > spg::kMaxSplits * 1024) return SPG_EUNSUPPORTED;
+  return SPG_OK;
+}
+
+spg_status spg_workspace_size(const spg_params* p, size_t* bytes) {
+  const spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!bytes) return SPG_EINVAL;
+  *bytes = spg::workspace_bytes(*p);
+  return SPG_OK;
+}
+
+spg_status sparse_page_meta_update(const spg_params* p, const void* k_pool, const void* k_scale,
+                                   const int32_t* page_table, const int32_t* seq_lens,
+                                   int32_t rebuild, void* minmax, uint8_t* sketch,
+                                   float* sketch_scale, const float* proj, void* ws,
+                                   size_t ws_bytes, spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!ok_ptr(k_pool) || !ok_ptr(page_table) || !ok_ptr(seq_lens)) return SPG_EINVAL;
+  if (p->kv_dtype == SPG_I8 && !ok_ptr(k_scale)) return SPG_EINVAL;
+  if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  return cuda_status(spg::launch_meta_update(*p, k_pool, k_scale, page_table, seq_lens, rebuild,
+                                             minmax, sketch, sketch_scale, proj, w.err,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spg_status sparse_page_score(const spg_params* p, const void* q, const int32_t* page_table,
+                             const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
+                             const float* sketch_scale, const float* proj, float* scores, void* ws,
+                             size_t ws_bytes, spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!ok_ptr(q) || !ok_ptr(page_table) || !ok_ptr(seq_lens) || !ok_ptr(scores)) return SPG_EINVAL;
+  if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  return cuda_status(spg::launch_score(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
+                                       proj, scores, w.err,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spg_status sparse_page_select(const spg_params* p, const void* q, const int32_t* page_table,
+                              const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
+                              const float* sketch_scale, const float* proj, int32_t* sel,
+                              int32_t* sel_cnt, void* ws, size_t ws_bytes, spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!ok_ptr(q) || !ok_ptr(page_table) || !ok_ptr(seq_lens) || !ok_ptr(sel) || !ok_ptr(sel_cnt))
+    return SPG_EINVAL;
+  if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = spg::launch_score(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
+                                    proj, w.scores, w.err, st);
+  if (e == cudaSuccess) e = spg::launch_topk(*p, w.scores, seq_lens, sel, sel_cnt, w.err, st);
+  return cuda_status(e);
+}
+
+spg_status sparse_decode_attention(const spg_params* p, const void* q, const void* k_pool,
+                                   const void* v_pool, const void* k_scale, const void* v_scale,
+                                   const int32_t* page_table, const int32_t* seq_lens,
+                                   const int32_t* sel, const int32_t* sel_cnt, float* out,
+                                   float* lse, void* ws, size_t ws_bytes, spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (p->selector == SPG_SEL_ALL) return SPG_EINVAL;  // needs a token budget for sel's shape
+  if (!ok_ptr(q) || !ok_ptr(page_table) || !ok_ptr(seq_lens) || !ok_ptr(sel) ||
+      !ok_ptr(sel_cnt) || !ok_ptr(out) || (lse && !aligned16(lse)))
+    return SPG_EINVAL;
+  if ((s = check_kv(p, k_pool, v_pool, k_scale, v_scale)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  return cuda_status(spg::launch_attention(*p, q, k_pool, v_pool, k_scale, v_scale, page_table,
+                                           seq_lens, sel, sel_cnt, out, lse, w,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const void* k_pool,
+                                       const void* v_pool, const void* k_scale,
+                                       const void* v_scale, const int32_t* page_table,
+                                       const int32_t* seq_lens, const void* minmax,
+                                       const uint8_t* sketch, const float* sketch_scale,
+                                       const float* proj, int32_t* sel, int32_t* sel_cnt,
+                                       float* out, float* lse, void* ws, size_t ws_bytes,
+                                       spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!ok_ptr(q) || !ok_ptr(page_table) || !ok_ptr(seq_lens) || !ok_ptr(sel) ||
+      !ok_ptr(sel_cnt) || !ok_ptr(out) || (lse && !aligned16(lse)))
+    return SPG_EINVAL;
+  if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
+  if ((s = check_kv(p, k_pool, v_pool, k_scale, v_scale)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = spg::launch_score(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
+                                    proj, w.scores, w.err, st);
+  if (e == cudaSuccess) e = spg::launch_topk(*p, w.scores, seq_lens, sel, sel_cnt, w.err, st);
+  if (e == cudaSuccess)
+    e = spg::launch_attention(*p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens, sel,
+                              sel_cnt, out, lse, w, st);
+  return cuda_status(e);
+}
+
+spg_status dense_decode_attention(const spg_params* p, const void* q, const void* k_pool,
+                                  const void* v_pool, const void* k_scale, const void* v_scale,
+                                  const int32_t* page_table, const int32_t* seq_lens, float* out,
+                                  float* lse, void* ws, size_t ws_bytes, spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!ok_ptr(q) || !ok_ptr(page_table) || !ok_ptr(seq_lens) || !ok_ptr(out) ||
+      (lse && !aligned16(lse)))
+    return SPG_EINVAL;
+  if ((s = check_kv(p, k_pool, v_pool, k_scale, v_scale)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  return cuda_status(spg::launch_attention(*p, q, k_pool, v_pool, k_scale, v_scale, page_table,
+                                           seq_lens, nullptr, nullptr, out, lse, w,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t stream) {
+  if (!ok_ptr(ws) || !bits) return SPG_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SPG_ECUDA;
+  if (cudaMemcpy(bits, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPG_ECUDA;
+  return SPG_OK;
+}
+
+spg_status spg_clear_device_error(void* ws, spg_stream_t stream) {
+  if (!ok_ptr(ws)) return SPG_EINVAL;
+  return cuda_status(
+      cudaMemsetAsync(ws, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

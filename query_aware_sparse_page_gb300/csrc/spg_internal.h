@@ -1,0 +1,48 @@
+// Host-side launchers shared between the kernel files and the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spg.h"
+
+namespace spg {
+
+// Workspace carved into its regions (all device pointers).
+struct Workspace {
+  int32_t* err;     // error word (header)
+  float* scores;    // [B][Hkv][MP]
+  float* pm;        // [B][Hq][kMaxSplits] running max (log2 domain)
+  float* pl;        // [B][Hq][kMaxSplits] running sum
+  float* pacc;      // [B][Hq][kMaxSplits][d] unnormalised output
+};
+
+size_t workspace_bytes(const spg_params& p);
+Workspace carve_workspace(const spg_params& p, void* ws);
+
+int n_sel_pages(const spg_params& p);
+int device_sm_count();
+int max_splits(const spg_params& p);
+
+cudaError_t launch_meta_update(const spg_params& p, const void* k_pool, const void* k_scale,
+                               const int32_t* page_table, const int32_t* seq_lens, int rebuild,
+                               void* minmax, uint8_t* sketch, float* sketch_scale,
+                               const float* proj, int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_score(const spg_params& p, const void* q, const int32_t* page_table,
+                         const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
+                         const float* sketch_scale, const float* proj, float* scores,
+                         int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_topk(const spg_params& p, const float* scores, const int32_t* seq_lens,
+                        int32_t* sel, int32_t* sel_cnt, int32_t* err, cudaStream_t stream);
+
+// sel == nullptr -> dense (every page of every sequence)
+cudaError_t launch_attention(const spg_params& p, const void* q, const void* k_pool,
+                             const void* v_pool, const void* k_scale, const void* v_scale,
+                             const int32_t* page_table, const int32_t* seq_lens,
+                             const int32_t* sel, const int32_t* sel_cnt, float* out, float* lse,
+                             const Workspace& ws, cudaStream_t stream);
+
+}  // namespace spg

@@ -1,0 +1,126 @@
+"""The C-ABI library builds, loads and exports every symbol include/spg.h
+declares; host-side validation answers without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spg.h")
+
+
+@pytest.fixture(scope="module")
+def spg():
+    from query_aware_sparse_page_gb300 import _build
+
+    _build.build()
+    import query_aware_sparse_page_gb300 as m
+
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:spg_status|int32_t|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["sparse_page_meta_update", "sparse_page_select", "sparse_decode_attention",
+              "sparse_decode_select_attend", "dense_decode_attention", "sparse_page_score",
+              "spg_workspace_size", "spg_validate"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(spg):
+    lib = ctypes.CDLL(spg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(spg):
+    assert spg.spg_abi_version() == 1
+    assert spg.status_str(0) == "ok"
+    assert spg.status_str(4) == "workspace too small"
+    assert spg.status_str(99) == "unknown status"
+
+
+def _valid(spg, **kw):
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                num_phys_pages=100, max_pages_per_seq=64, kv_dtype="f16", selector="quest",
+                token_budget=16 * 8, n_sink_pages=1, n_recent_pages=1)
+    base.update(kw)
+    return spg.make_params(**base)
+
+
+def test_every_workload_validates(spg):
+    from synth import WORKLOADS, make_inputs, scaled
+
+    for w in WORKLOADS.values():
+        small = scaled(w, batch=1, seq_len=w.page_size * 4, seq_range=None)
+        inp = make_inputs(small)
+        p = spg.params_for(inp)
+        assert spg.spg_validate(p) == 0, w.name
+        assert spg.spg_workspace_size(p) > 0
+
+
+@pytest.mark.parametrize("change, status", [
+    (dict(num_q_heads=7), 1),                 # Hq % Hkv
+    (dict(head_dim=48), 1),                   # not a multiple of 32
+    (dict(head_dim=96), 2),                   # valid, not built
+    (dict(num_q_heads=6), 2),                 # group of 3
+    (dict(page_size=12), 1),
+    (dict(page_size=256), 1),
+    (dict(token_budget=100), 1),              # not a multiple of the page size
+    (dict(token_budget=16), 1),               # budget below the forced pages
+    (dict(n_sink_pages=-1), 1),
+    (dict(kv_dtype="i8"), 2),                 # Quest over int8 is not built
+    (dict(kv_dtype="bf16", q_dtype="f16"), 1),
+    (dict(selector="sketch", sketch_dim=8), 1),
+    (dict(selector="sketch", n_recent_pages=0), 1),
+    (dict(softmax_scale=-1.0), 1),
+    (dict(max_pages_per_seq=100000), 2),      # beyond the shared-memory top-k
+    (dict(batch=0), 1),
+])
+def test_validation(spg, change, status):
+    assert spg.spg_validate(_valid(spg, **change)) == status
+
+
+def test_sketch_int8_and_dense_params_are_valid(spg):
+    assert spg.spg_validate(_valid(spg, selector="sketch", kv_dtype="i8", page_size=64)) == 0
+    assert spg.spg_validate(_valid(spg, selector="all", token_budget=0, n_sink_pages=0,
+                                   n_recent_pages=0)) == 0
+
+
+def test_null_arguments_rejected_on_host(spg):
+    p = _valid(spg)
+    L = spg.LIB
+    null = None
+    assert L.sparse_page_select(ctypes.byref(p), null, null, null, null, null, null, null, null,
+                                null, null, 0, null) == 1
+    assert L.sparse_decode_attention(ctypes.byref(p), *([null] * 12), 0, null) == 1
+    assert L.dense_decode_attention(ctypes.byref(p), *([null] * 10), 0, null) == 1
+    assert L.sparse_page_meta_update(ctypes.byref(p), null, null, null, null, 0, null, null, null,
+                                     null, null, 0, null) == 1
+    assert L.spg_validate(None) == 1
+    n = ctypes.c_size_t(0)
+    assert L.spg_workspace_size(ctypes.byref(_valid(spg, head_dim=48)), ctypes.byref(n)) == 1
+
+
+def test_workspace_grows_with_the_problem(spg):
+    a = spg.spg_workspace_size(_valid(spg))
+    b = spg.spg_workspace_size(_valid(spg, batch=4))
+    c = spg.spg_workspace_size(_valid(spg, max_pages_per_seq=4096))
+    assert a < b and a < c
+
+
+def test_binding_refuses_host_tensors(spg):
+    import torch
+
+    p = _valid(spg)
+    t = torch.zeros(16)
+    with pytest.raises(ValueError):
+        spg.sparse_page_score(p, t, t, t, t, scores=t, ws=torch.zeros(16, dtype=torch.uint8))

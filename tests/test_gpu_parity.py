@@ -1,0 +1,281 @@
+"""CUDA path vs oracle, element by element, through the C ABI.
+
+Small cases (every unit checked, several tiles and ragged tails) for each
+workload recipe, edge cases, and the full-size workloads on sampled units
+in the launch configuration the benchmark times.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode, quest, sketch as osk
+from synth import get_workload, make_inputs, scaled
+
+from conftest import oracle_inputs, oracle_params, to_numpy
+from gpu_helpers import TOL_OUT, check_unit, gpu_selection, run_step
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _spg():
+    import query_aware_sparse_page_gb300 as spg
+
+    return spg
+
+
+SMALL = {
+    "tiny": scaled(get_workload("tiny-quest-gqa4-1k")),
+    "tiny-ragged": scaled(get_workload("tiny-quest-gqa4-1k"), seq_len=1000 + 7),
+    "mha": scaled(get_workload("llama2-7b-mha-32k"), num_q_heads=4, num_kv_heads=4, seq_len=4096 + 9,
+                  n_sel_pages=32, needles_per_head=4),
+    "gqa-ragged": scaled(get_workload("gqa-serving-b8-4k-64k"), batch=3, num_q_heads=8, num_kv_heads=2,
+                         seq_range=(100, 3000), n_sel_pages=24),
+    "sals-4x": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                      seq_len=64 * 30 + 17, n_sel_pages=9),
+    "sals-6x-full-tail": scaled(get_workload("sals-int8-b16-10k-6x"), batch=2, num_q_heads=8,
+                                num_kv_heads=2, seq_len=64 * 24, n_sel_pages=5),
+    "long-d64-g8": scaled(get_workload("long-scan-b4-128k"), batch=2, num_q_heads=16, num_kv_heads=2,
+                          head_dim=64, seq_len=16 * 700 + 3, needles_per_head=8, n_sel_pages=40),
+    "gqa2-f16": scaled(get_workload("tiny-quest-gqa4-1k"), num_q_heads=4, num_kv_heads=2, head_dim=128,
+                       seq_len=2000, n_sel_pages=20, n_sink=2, n_recent=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_workload_every_unit(name):
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    p, bufs, err = run_step(inp)
+    assert err == 0
+    prm = oracle_params(w)
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            check_unit(inp, prm, bufs, b, h, TOL_OUT[w.kv_dtype])
+
+
+@pytest.mark.parametrize("name", ["tiny", "mha", "gqa-ragged", "sals-4x"])
+def test_separate_calls_equal_fused(name):
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    _, b1, _ = run_step(inp, fused=True)
+    _, b2, _ = run_step(inp, fused=False)
+    assert torch.equal(b1.sel, b2.sel) and torch.equal(b1.sel_cnt, b2.sel_cnt)
+    assert torch.equal(b1.out, b2.out) and torch.equal(b1.lse, b2.lse)
+
+
+@pytest.mark.parametrize("name", ["tiny-ragged", "mha", "gqa-ragged", "sals-4x", "long-d64-g8"])
+def test_dense_baseline(name):
+    spg = _spg()
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    bufs = spg.alloc_buffers(p, DEV)
+    spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                               inp.page_table, inp.seq_lens, bufs.out, bufs.lse, bufs.ws)
+    assert spg.spg_read_device_error(bufs.ws) == 0
+    oi = oracle_inputs(inp)
+    prm = oracle_params(w, selector="all")
+    res = decode.decode_step(oi, prm)
+    G = w.group
+    tol = TOL_OUT[w.kv_dtype]
+    for (b, h), out in res["out"].items():
+        gout = bufs.out[b, h * G : (h + 1) * G].cpu().numpy()
+        glse = bufs.lse[b, h * G : (h + 1) * G].cpu().numpy()
+        assert np.abs(gout - out).max() <= tol
+        assert np.abs(glse - res["lse"][(b, h)]).max() <= tol
+
+
+def test_full_budget_sparse_equals_dense():
+    """Selecting every page reproduces dense attention (100% retention check)."""
+    spg = _spg()
+    w = scaled(get_workload("tiny-quest-gqa4-1k"), seq_len=777, n_sel_pages=64)
+    inp = make_inputs(w, device=DEV)
+    _, bufs, _ = run_step(inp)
+    p = spg.params_for(inp)
+    d = spg.alloc_buffers(p, DEV)
+    spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, None, None, inp.page_table,
+                               inp.seq_lens, d.out, d.lse, d.ws)
+    assert gpu_selection(bufs, 0, 0) == list(range(49))
+    assert (bufs.out - d.out).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("name", ["tiny-ragged", "mha", "gqa-ragged", "long-d64-g8"])
+def test_minmax_rebuild_bit_exact(name):
+    spg = _spg()
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    bufs = spg.alloc_buffers(p, DEV)
+    spg.sparse_page_meta_update(p, inp.k_pool, None, inp.page_table, inp.seq_lens, 1, bufs.minmax,
+                                None, None, None, bufs.ws)
+    ref = quest.page_minmax(to_numpy(inp.k_pool), to_numpy(inp.page_table), to_numpy(inp.seq_lens),
+                            w.page_size)
+    got = to_numpy(bufs.minmax).astype(np.float64)
+    used = ~np.isnan(ref[:, 0, 0, 0])
+    assert np.array_equal(got[used], ref[used])
+
+
+def _append_sequence(spg, inp, p, bufs, lens_final):
+    """Append tokens one by one (seq_lens 1..L) through the append entry point."""
+    for t in range(1, int(max(lens_final)) + 1):
+        lens = torch.clamp(torch.tensor(lens_final, dtype=torch.int32), max=t).to(DEV)
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, lens, 0,
+                                    bufs.minmax, bufs.sketch, bufs.sketch_scale, inp.proj, bufs.ws)
+
+
+def test_minmax_append_equals_rebuild():
+    spg = _spg()
+    w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=3, num_q_heads=8, num_kv_heads=2,
+               seq_range=(20, 90), n_sel_pages=4)
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    a = spg.alloc_buffers(p, DEV)
+    r = spg.alloc_buffers(p, DEV)
+    a.minmax.fill_(7.0)  # stale content from a recycled page must not leak
+    _append_sequence(spg, inp, p, a, inp.seq_lens.cpu().tolist())
+    spg.sparse_page_meta_update(p, inp.k_pool, None, inp.page_table, inp.seq_lens, 1, r.minmax, None,
+                                None, None, r.ws)
+    ref = quest.page_minmax(to_numpy(inp.k_pool), to_numpy(inp.page_table), to_numpy(inp.seq_lens),
+                            w.page_size)
+    used = ~np.isnan(ref[:, 0, 0, 0])
+    assert torch.equal(a.minmax[torch.from_numpy(used).to(DEV)], r.minmax[torch.from_numpy(used).to(DEV)])
+    assert spg.spg_read_device_error(a.ws) == 0
+
+
+@pytest.mark.parametrize("name", ["sals-4x", "sals-6x-full-tail"])
+def test_sketch_codes_bit_exact(name):
+    spg = _spg()
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    bufs = spg.alloc_buffers(p, DEV)
+    spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 1, None,
+                                bufs.sketch, bufs.sketch_scale, inp.proj, bufs.ws)
+    kp, ks, pt, proj = to_numpy(inp.k_pool), to_numpy(inp.k_scale), to_numpy(inp.page_table), to_numpy(inp.proj)
+    sk_gpu = bufs.sketch.cpu().numpy()
+    sc_gpu = bufs.sketch_scale.cpu().numpy()
+    n_checked = 0
+    for b, L in enumerate(to_numpy(inp.seq_lens)):
+        for blk in range(int(L) // w.page_size):
+            phys = int(pt[b, blk])
+            for h in range(w.num_kv_heads):
+                codes, scale = osk.build_sketch(osk.dequant(kp[phys, h], ks[phys, h]), proj)
+                assert np.array_equal(osk.unpack_int4(sk_gpu[phys, h]), codes)
+                assert sc_gpu[phys, h] == scale
+                n_checked += 1
+    assert n_checked > 0
+
+
+def test_sketch_append_equals_rebuild():
+    spg = _spg()
+    w = scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+               seq_len=64 * 3 + 5, n_sel_pages=2)
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    a = spg.alloc_buffers(p, DEV)
+    r = spg.alloc_buffers(p, DEV)
+    _append_sequence(spg, inp, p, a, inp.seq_lens.cpu().tolist())
+    spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 1, None,
+                                r.sketch, r.sketch_scale, inp.proj, r.ws)
+    assert torch.equal(a.sketch, r.sketch) and torch.equal(a.sketch_scale, r.sketch_scale)
+
+
+def test_edge_sequences():
+    """Empty, one-token, page-aligned, and shorter-than-budget sequences."""
+    w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=6, num_q_heads=8, num_kv_heads=2,
+               seq_range=(1, 2), n_sel_pages=6)
+    inp = make_inputs(w, device=DEV, seq_lens=[0, 1, 16, 17, 95, 1600])
+    p, bufs, err = run_step(inp)
+    assert err == 0
+    prm = oracle_params(w)
+    for b in range(6):
+        for h in range(2):
+            check_unit(inp, prm, bufs, b, h, TOL_OUT[w.kv_dtype])
+    assert bufs.sel_cnt[0].tolist() == [0, 0]
+    assert (bufs.out[0] == 0).all() and torch.isneginf(bufs.lse[0]).all()
+
+
+def test_all_equal_scores_take_lowest_pages():
+    """Identical pages tie everywhere: the lowest candidate pages win."""
+    spg = _spg()
+    w = scaled(get_workload("tiny-quest-gqa4-1k"), seq_len=16 * 40, n_sel_pages=7, needles_per_head=0)
+    inp = make_inputs(w, device=DEV)
+    inp.k_pool[:] = inp.k_pool[0:1, :, :, :]  # every page the same
+    _, bufs, _ = run_step(inp)
+    assert gpu_selection(bufs, 0, 0) == [0, 1, 2, 3, 4, 5, 39]
+
+
+@pytest.mark.parametrize("name", ["tiny", "long-d64-g8"])
+def test_needle_pages_selected(name):
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    _, bufs, _ = run_step(inp)
+    for (b, h), pos in inp.needles.items():
+        pages = {t // w.page_size for t in pos}
+        assert pages <= set(gpu_selection(bufs, b, h))
+
+
+def test_bad_page_id_is_reported_not_read():
+    spg = _spg()
+    w = SMALL["tiny"]
+    inp = make_inputs(w, device=DEV)
+    inp.page_table[0, 5] = inp.num_phys_pages + 1000  # outside the pool
+    p, bufs, err = run_step(inp)
+    assert err & spg.DEVERR_PAGE_ID
+    spg.spg_clear_device_error(bufs.ws)
+    assert spg.spg_read_device_error(bufs.ws) == 0
+
+
+def test_host_validation_errors():
+    spg = _spg()
+    w = SMALL["tiny"]
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    bufs = spg.alloc_buffers(p, DEV)
+    with pytest.raises(spg.SpgError) as e:  # workspace too small
+        spg.sparse_page_select(p, inp.q, inp.page_table, inp.seq_lens, bufs.minmax, sel=bufs.sel,
+                               sel_cnt=bufs.sel_cnt, ws=bufs.ws[:256])
+    assert e.value.status == 4
+    with pytest.raises(spg.SpgError) as e:  # misaligned query pointer
+        spg.sparse_page_select(p, inp.q.view(-1)[1:], inp.page_table, inp.seq_lens, bufs.minmax,
+                               sel=bufs.sel, sel_cnt=bufs.sel_cnt, ws=bufs.ws)
+    assert e.value.status == 1
+
+
+# ---- full sizes, sampled units, benchmark launch configuration ----------------
+FULL = ["llama2-7b-mha-32k", "gqa-serving-b8-4k-64k", "sals-int8-b16-10k-4x",
+        "sals-int8-b16-10k-6x", "long-scan-b4-128k"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_units(name):
+    w = get_workload(name)
+    inp = make_inputs(w, device=DEV)
+    p, bufs, err = run_step(inp)
+    assert err == 0
+    prm = oracle_params(w)
+    rng = np.random.default_rng(7)
+    units = {(0, 0), (w.batch - 1, w.num_kv_heads - 1)}
+    while len(units) < 4:
+        units.add((int(rng.integers(w.batch)), int(rng.integers(w.num_kv_heads))))
+    for b, h in sorted(units):
+        gsel = check_unit(inp, prm, bufs, b, h, TOL_OUT[w.kv_dtype])
+        if (b, h) in inp.needles:
+            assert {t // w.page_size for t in inp.needles[(b, h)]} <= set(gsel)
+    # every unit: count, order and forced pages (properties that hold at any size)
+    cnt = bufs.sel_cnt.cpu().numpy()
+    sel = bufs.sel.cpu().numpy()
+    lens = to_numpy(inp.seq_lens)
+    for b in range(w.batch):
+        P = -(-int(lens[b]) // w.page_size)
+        for h in range(w.num_kv_heads):
+            s = sel[b, h, : cnt[b, h]]
+            assert cnt[b, h] == min(w.n_sel_pages, P)
+            assert np.all(np.diff(s) > 0) and s[0] >= 0 and s[-1] == P - 1
+            if w.n_sink:
+                assert s[0] == 0
