@@ -13,9 +13,9 @@ HEADER = os.path.join(ROOT, "include", "spg.h")
 
 @pytest.fixture(scope="module")
 def spg():
-    from query_aware_sparse_page_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__.build()
     import query_aware_sparse_page_gb300 as m
 
     return m
