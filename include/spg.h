@@ -201,6 +201,39 @@ spg_status dense_decode_attention(const spg_params* p, const void* q, const void
                                   const int32_t* page_table, const int32_t* seq_lens, float* out,
                                   float* lse, void* ws, size_t ws_bytes, spg_stream_t stream);
 
+/* Bytes of the library-owned scratch array behind
+ * sparse_decode_attention_noalloc (16 MiB).  A call needs
+ * 256 + 512 * rows * (head_dim + 2) bytes (each region rounded up to 256),
+ * rows = batch * num_q_heads: at most 252 rows at head_dim 128, 496 at 64. */
+#define SPG_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* sparse_decode_attention for callers that cannot allocate device memory
+ * (no counterpart in the source papers: it exists for embedding this
+ * library).  Plugins run by a host framework that owns all device memory
+ * and gives them no allocator or workspace, and serving loops that forbid
+ * cudaMalloc after start-up, cannot supply the workspace the other entry
+ * points take.  This one takes the same arguments minus the workspace and
+ * keeps its scratch (split partials, an error word) in one array of
+ * SPG_NOALLOC_SCRATCH_BYTES of device memory owned by the library, which
+ * every GPU that loads the library holds until the process exits.
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that
+ *   first call before any stream capture.
+ * - Returns SPG_EWORKSPACE when the problem's partials do not fit the array
+ *   (see SPG_NOALLOC_SCRATCH_BYTES), before launching anything.
+ * - All calls on a device share the array and leave their contents in it:
+ *   calls whose kernels overlap on the GPU (unordered streams) race and
+ *   corrupt each other's results.  Order them on one stream.
+ * - Device-detected faults (bad page ids) are skipped as in the other entry
+ *   points, but this entry point has no error word the caller can read. */
+spg_status sparse_decode_attention_noalloc(const spg_params* p, const void* q, const void* k_pool,
+                                           const void* v_pool, const void* k_scale,
+                                           const void* v_scale, const int32_t* page_table,
+                                           const int32_t* seq_lens, const int32_t* sel,
+                                           const int32_t* sel_cnt, float* out, float* lse,
+                                           spg_stream_t stream);
+
 /* Waits for `stream`, then copies the workspace error word to *bits. */
 spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t stream);
 
