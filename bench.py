@@ -147,6 +147,17 @@ def selection_stats(w, inp, sel, sel_cnt):
 
 
 # ----------------------------------------------------------------- our GPU arm
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's value (the job finishes when its last rank does)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, world, rank, local):
     import torch.distributed as dist
 
@@ -165,16 +176,64 @@ def run_ours(args, world, rank, local):
                                     bufs.minmax, bufs.sketch, bufs.sketch_scale, inp.proj, bufs.ws)
         layers.append((inp, p, bufs))
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream(dev)
 
-    def step(i):
-        inp, p, b = layers[i % R]
+    # the entry points of one step, per layer
+    def op_meta(l):
+        inp, p, b = layers[l]
         spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 0,
                                     b.minmax, b.sketch, b.sketch_scale, inp.proj, b.ws)
+
+    def op_select_attend(l):
+        inp, p, b = layers[l]
         spg.sparse_decode_select_attend(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
                                         inp.page_table, inp.seq_lens, b.minmax, b.sketch,
                                         b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.out, b.lse,
                                         b.ws)
+
+    def op_step(l):
+        op_meta(l)
+        op_select_attend(l)
+
+    def op_score(l):
+        inp, p, b = layers[l]
+        spg.sparse_page_score(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                              b.sketch_scale, inp.proj, b.scores, b.ws)
+
+    def op_select(l):
+        inp, p, b = layers[l]
+        spg.sparse_page_select(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                               b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.ws)
+
+    def op_attn(l):
+        inp, p, b = layers[l]
+        spg.sparse_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                    inp.page_table, inp.seq_lens, b.sel, b.sel_cnt, b.out, b.lse,
+                                    b.ws)
+
+    def op_dense(l):
+        inp, p, b = layers[l]
+        spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                   inp.page_table, inp.seq_lens, b.out, b.lse, b.ws)
+
+    ops = {"step": op_step, "meta": op_meta, "score": op_score, "select": op_select,
+           "attn": op_attn, "dense": op_dense}
+    for l in range(R):  # eager warm-up of every entry point (kernel attributes, caches)
+        for f in ops.values():
+            f(l)
+    op_step(0)  # leave layer 0 with the step's own selection
+    torch.cuda.synchronize()
+
+    # one CUDA graph per (entry point, layer): a step replays as one launch
+    graphs = {}
+    for name, f in ops.items():
+        graphs[name] = []
+        for l in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                f(l)
+            graphs[name].append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
 
     def barrier():
         if world > 1:
@@ -190,59 +249,31 @@ def run_ours(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms / K
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / K
+
+    def replay(name):
+        gs = graphs[name]
+        return lambda i: gs[i % R].replay()
 
     K, W = args.steps, args.warmup
-    for i in range(W):
-        step(i)
     clocks = ClockSampler(local)
     clocks.start()
-    ms_step = timed(step, K)
-    clock_info = clocks.stop()
-
-    # per-kernel attribution: the same step split into its entry points, events between
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    torch.cuda.synchronize()
-    for i in range(K):
-        inp, p, b = layers[i % R]
-        ev[i][0].record(stream)
-        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 0,
-                                    b.minmax, b.sketch, b.sketch_scale, inp.proj, b.ws)
-        ev[i][1].record(stream)
-        spg.sparse_page_select(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
-                               b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.ws)
-        ev[i][2].record(stream)
-        spg.sparse_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
-                                    inp.page_table, inp.seq_lens, b.sel, b.sel_cnt, b.out, b.lse,
-                                    b.ws)
-        ev[i][3].record(stream)
-    torch.cuda.synchronize()
-    ph = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(3)] for i in range(K)]).mean(0)
-    # the select phase alone on its score kernel (one launch per call)
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-    e_s[0].record(stream)
-    for i in range(K):
-        inp, p, b = layers[i % R]
-        spg.sparse_page_score(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
-                              b.sketch_scale, inp.proj, b.scores, b.ws)
-        e_s[i + 1].record(stream)
-    torch.cuda.synchronize()
-    ms_score = float(np.mean([e_s[i].elapsed_time(e_s[i + 1]) for i in range(K)]))
-
-    # dense baseline over the same caches
-    def dense(i):
-        inp, p, b = layers[i % R]
-        spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
-                                   inp.page_table, inp.seq_lens, b.out, b.lse, b.ws)
-
     for i in range(W):
-        dense(i)
-    ms_dense = timed(dense, K)
+        graphs["step"][i % R].replay()
+    t_end = time.perf_counter() + args.soak
+    i = 0
+    while time.perf_counter() < t_end:  # keep the GPU loaded while clocks are sampled
+        graphs["step"][i % R].replay()
+        i += 1
+    ms_step = timed(replay("step"), K)
+    clock_info = clocks.stop()
+    clock_info["window"] = "warm-up, soak and timed steps"
+
+    # per-entry-point durations (each replayed K times, layers rotating)
+    ms = {name: timed(replay(name), K) for name in ("meta", "score", "select", "attn", "dense")}
+    ms_topk = max(ms["select"] - ms["score"], 0.0)
+    # the same step issued eagerly through the Python binding (host-issue bound)
+    ms_eager = timed(lambda i: op_step(i % R), max(K // 4, 10))
 
     # bytes
     inp0, p0, b0 = layers[0]
@@ -255,18 +286,17 @@ def run_ours(args, world, rank, local):
     dense_b = dense_tok * 2 * (w.head_dim * kvb + (2 if w.kv_dtype == "i8" else 0)) + small_b
     peak, peak_kind = measured_peaks()
 
-    # roofline of the dominant phase
-    phases = {"meta_update": ph[0], "select(score+topk)": ph[1], "attention(attn+combine)": ph[2]}
-    dom = max(phases, key=phases.get)
-    if dom.startswith("attention"):
-        dom_bytes, dom_ms, kname = kv_b + small_b, ph[2], "k_attn+k_combine"
-    elif dom.startswith("select"):
-        dom_bytes, dom_ms, kname = meta_b, ms_score, "k_quest_score" if w.selector == "quest" else "k_sketch_score"
-    else:
-        dom_bytes, dom_ms, kname = 0, ph[0], "meta"
+    # roofline of the dominant kernel (one launch per entry point timed)
+    score_name = "k_quest_score" if w.selector == "quest" else "k_sketch_score"
+    kernels = {
+        "k_attn": (ms["attn"], kv_b + small_b),
+        score_name: (ms["score"], meta_b),
+        "k_topk": (ms_topk, cand * 4 + sel_pages * 4),
+    }
+    kname = max(kernels, key=lambda k: kernels[k][0])
+    dom_ms, dom_bytes = kernels[kname]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else 0.0
 
-    # end to end through the public API with host buffers
     e2e = run_e2e(args, spg, layers, stream, world, dev)
 
     steps_s = world * 1000.0 / ms_step
@@ -293,20 +323,24 @@ def run_ours(args, world, rank, local):
             "layers_rotated": R,
             "l2": f"inputs larger than L2: {R} rotating cache replicas, each step reads "
                   f"{total_b / 1e6:.1f} MB of a distinct replica",
+            "launch": "one CUDA graph per layer replays the step's entry points",
             "parallelism": "replicas" if world > 1 else "single",
         },
         "hbm_gbs_effective": round(gbs, 1),
         "hbm_frac_nominal": round(gbs / world / NOMINAL_HBM_GBS, 4),
         "hbm_frac_measured": round(gbs / world / peak, 4),
-        "bytes_per_step": {"metadata": meta_b, "selected_kv": kv_b, "q_out_idx": small_b, "total": total_b},
+        "bytes_per_step": {"metadata": meta_b, "selected_kv": kv_b, "q_out_idx": small_b,
+                           "total": total_b},
         "dense": {
-            "steps_per_s": round(world * 1000.0 / ms_dense, 2),
-            "ms_per_step": round(ms_dense, 5),
+            "steps_per_s": round(world * 1000.0 / ms["dense"], 2),
+            "ms_per_step": round(ms["dense"], 5),
             "bytes_per_step": dense_b,
-            "hbm_gbs": round(dense_b / (ms_dense * 1e-3) / 1e9, 1),
-            "speedup_sparse_vs_dense": round(ms_dense / ms_step, 3),
+            "hbm_gbs": round(dense_b / (ms["dense"] * 1e-3) / 1e9, 1),
+            "speedup_sparse_vs_dense": round(ms["dense"] / ms_step, 3),
         },
-        "phase_ms": {k: round(float(v), 5) for k, v in phases.items()},
+        "kernel_ms": {"meta_append": round(ms["meta"], 5), score_name: round(ms["score"], 5),
+                      "k_topk(select-score)": round(ms_topk, 5), "k_attn": round(ms["attn"], 5)},
+        "eager_steps_per_s": round(world * 1000.0 / ms_eager, 2),
         "roofline": {
             "kernel": kname,
             "bound": "hbm",
@@ -321,7 +355,7 @@ def run_ours(args, world, rank, local):
         },
         "clocks": clock_info,
         "e2e": e2e,
-        "gpu_launches": K * (5 if w.selector != "all" else 2),
+        "gpu_launches": K * 4,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, layers[0][0], budget_s=args.cpu_seconds)
@@ -500,8 +534,9 @@ def run_reference(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--soak", type=float, default=0.5, help="seconds of untimed steps before timing")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--layers", type=int, default=8)

@@ -203,8 +203,9 @@ spg_status dense_decode_attention(const spg_params* p, const void* q, const void
 
 /* Bytes of the library-owned scratch array behind
  * sparse_decode_attention_noalloc (16 MiB).  A call needs
- * 256 + 512 * rows * (head_dim + 2) bytes (each region rounded up to 256),
- * rows = batch * num_q_heads: at most 252 rows at head_dim 128, 496 at 64. */
+ * 256 + 4 * units + 512 * rows * (head_dim + 2) bytes (each region rounded
+ * up to 256), rows = batch * num_q_heads, units = batch * num_kv_heads: at
+ * most 252 rows at head_dim 128, 496 at 64. */
 #define SPG_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* sparse_decode_attention for callers that cannot allocate device memory

@@ -26,9 +26,10 @@ int device_sm_count() {
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t workspace_bytes(const spg_params& p) {
-  const size_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads, d = p.head_dim;
-  const size_t MP = p.max_pages_per_seq;
+  const size_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+  const size_t d = p.head_dim, MP = p.max_pages_per_seq;
   size_t off = 256;                                      // header: error word
+  off += align256(sizeof(int32_t) * B * Hkv);            // split arrival counters
   off += align256(sizeof(float) * B * Hkv * MP);         // scores
   off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pm
   off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pl
@@ -43,6 +44,8 @@ Workspace carve_workspace(const spg_params& p, void* ws) {
   Workspace w{};
   w.err = reinterpret_cast<int32_t*>(base);
   size_t off = 256;
+  w.counters = reinterpret_cast<int32_t*>(base + off);
+  off += align256(sizeof(int32_t) * B * Hkv);
   w.scores = reinterpret_cast<float*>(base + off);
   off += align256(sizeof(float) * B * Hkv * MP);
   w.pm = reinterpret_cast<float*>(base + off);

@@ -21,7 +21,10 @@
 // drains the copies this warp issued (bounded again) and stops.
 //
 // Partials per (batch, q-head, split): running max m (log2 domain, scale
-// folded in), running sum l, unnormalised accumulator acc[d].
+// folded in), running sum l, unnormalised accumulator acc[d].  The last CTA
+// of a unit to arrive (an atomic counter per unit in the workspace, reset by
+// that CTA) merges the unit's splits and writes out and lse, so one launch
+// does the whole attention.
 #include <float.h>
 
 #include "spg_common.cuh"
@@ -45,6 +48,9 @@ struct AttnArgs {
   float* pm;
   float* pl;
   float* pacc;
+  int32_t* counters;  // split arrivals per unit, zero between launches
+  float* out;
+  float* lse;
   int32_t* err;
   int Hkv, S, MP, n_phys, n_sel, pages_per_split;
   float scale_log2;
@@ -296,46 +302,50 @@ __global__ void __launch_bounds__(W * 32) k_attn(const AttnArgs a) {
       a.pl[pidx] = Ls;
     }
   }
-}
 
-// One warp per (batch, q-head) row: merge the splits by log-sum-exp.
-template <int D>
-__global__ void k_combine(const float* __restrict__ pm, const float* __restrict__ pl,
-                          const float* __restrict__ pacc, float* __restrict__ out,
-                          float* __restrict__ lse, int rows, int n_split) {
-  constexpr int CPL = D / 32;
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float* m = pm + static_cast<size_t>(row) * kMaxSplits;
-  const float* l = pl + static_cast<size_t>(row) * kMaxSplits;
-  float M = -INFINITY;
-  for (int s = lane; s < n_split; s += 32) M = fmaxf(M, m[s]);
-  M = warp_max(M);
-  float o[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) o[c] = 0.f;
-  float Ls = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_split; ++s) {
-      const float f = exp2f(m[s] - M);
-      Ls = fmaf(l[s], f, Ls);
-      const float* A = pacc + (static_cast<size_t>(row) * kMaxSplits + s) * D + lane * CPL;
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) o[c] = fmaf(A[c], f, o[c]);
-    }
+  // The last CTA of the unit to finish merges every split by log-sum-exp
+  // (SALS AICPU Tiling, challenge 2: the reduction of a row split across
+  // cores).  Writers publish their partials with a device-scope fence before
+  // counting themselves in; no CTA ever waits for another.
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(&a.counters[unit], 1);
+    s_last = (prev == static_cast<int>(gridDim.x) - 1);
   }
-  float* orow = out + static_cast<size_t>(row) * D + lane * CPL;
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int n_split = gridDim.x;
+  for (int g = warp; g < G; g += W) {
+    const size_t row = static_cast<size_t>(b) * Hq + h * G + g;
+    const float* pmr = a.pm + row * kMaxSplits;
+    const float* plr = a.pl + row * kMaxSplits;
+    float M = -INFINITY;
+    for (int sp = lane; sp < n_split; sp += 32) M = fmaxf(M, __ldcg(pmr + sp));
+    M = warp_max(M);
+    float o[CPL];
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) orow[c] = o[c] * inv;
-  if (lse && lane == 0) lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+    float Ls = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < n_split; ++sp) {
+        const float f = exp2f(__ldcg(pmr + sp) - M);
+        Ls = fmaf(__ldcg(plr + sp), f, Ls);
+        const float* A = a.pacc + (row * kMaxSplits + sp) * D + lane * CPL;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) o[c] = fmaf(__ldcg(A + c), f, o[c]);
+      }
+    }
+    float* orow = a.out + row * D + lane * CPL;
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) orow[c] = o[c] * inv;
+    if (a.lse && lane == 0) a.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+  }
+  if (threadIdx.x == 0) a.counters[unit] = 0;  // ready for the next call
 }
-
-struct SplitPlan {
-  int n_split;
-  int pages_per_split;
-};
 
 template <typename T, typename TQ, int D, int G>
 cudaError_t attn_typed(const spg_params& p, const AttnArgs& a0, int pages_upper, float* out,
@@ -366,13 +376,10 @@ cudaError_t attn_typed(const spg_params& p, const AttnArgs& a0, int pages_upper,
     if (e != cudaSuccess) return e;
     configured = static_cast<int>(smem);
   }
+  a.out = out;
+  a.lse = lse;
   dim3 grid(n_split, units);
   kern<<<grid, W * 32, smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int rows = p.batch * p.num_q_heads;
-  k_combine<D><<<(rows * 32 + 255) / 256, 256, 0, st>>>(a.pm, a.pl, a.pacc, out, lse, rows,
-                                                         n_split);
   return cudaGetLastError();
 }
 
@@ -408,6 +415,7 @@ cudaError_t launch_attention(const spg_params& p, const void* q, const void* k_p
   a.pm = ws.pm;
   a.pl = ws.pl;
   a.pacc = ws.pacc;
+  a.counters = ws.counters;
   a.err = ws.err;
   a.Hkv = p.num_kv_heads;
   a.S = p.page_size;

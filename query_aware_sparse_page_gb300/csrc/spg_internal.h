@@ -12,6 +12,7 @@ namespace spg {
 // Workspace carved into its regions (all device pointers).
 struct Workspace {
   int32_t* err;     // error word (header)
+  int32_t* counters;  // [B][Hkv] split arrivals of the attention kernel; zero between calls
   float* scores;    // [B][Hkv][MP]
   float* pm;        // [B][Hq][kMaxSplits] running max (log2 domain)
   float* pl;        // [B][Hq][kMaxSplits] running sum

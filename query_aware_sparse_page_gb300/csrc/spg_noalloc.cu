@@ -38,10 +38,13 @@ std::mutex g_scratch_mu;
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// bytes of scratch one call needs: error word header + split partials
+// bytes of scratch one call needs: error word header, split arrival
+// counters, split partials
 size_t scratch_needed(const spg_params& p) {
   const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads;
-  return 256 + 2 * round256(sizeof(float) * rows * spg::kMaxSplits) +
+  const size_t units = static_cast<size_t>(p.batch) * p.num_kv_heads;
+  return 256 + round256(sizeof(int32_t) * units) +
+         2 * round256(sizeof(float) * rows * spg::kMaxSplits) +
          round256(sizeof(float) * rows * spg::kMaxSplits * p.head_dim);
 }
 
@@ -84,6 +87,9 @@ extern "C" spg_status sparse_decode_attention_noalloc(
   w.err = reinterpret_cast<int32_t*>(b);
   w.scores = nullptr;  // attention does not score pages
   size_t off = 256;
+  const size_t units = static_cast<size_t>(p->batch) * p->num_kv_heads;
+  w.counters = reinterpret_cast<int32_t*>(b + off);
+  off += round256(sizeof(int32_t) * units);
   w.pm = reinterpret_cast<float*>(b + off);
   off += round256(sizeof(float) * rows * spg::kMaxSplits);
   w.pl = reinterpret_cast<float*>(b + off);
@@ -91,8 +97,10 @@ extern "C" spg_status sparse_decode_attention_noalloc(
   w.pacc = reinterpret_cast<float*>(b + off);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the error word is the only part read before it is written: start it at zero
-  if (cudaMemsetAsync(w.err, 0, sizeof(int32_t), st) != cudaSuccess) return SPG_ECUDA;
+  // the error word and the split arrival counters are read before they are
+  // written: start them at zero (header and counters are contiguous)
+  if (cudaMemsetAsync(b, 0, 256 + round256(sizeof(int32_t) * units), st) != cudaSuccess)
+    return SPG_ECUDA;
   const cudaError_t e = spg::launch_attention(*p, q, k_pool, v_pool, k_scale, v_scale, page_table,
                                               seq_lens, sel, sel_cnt, out, lse, w, st);
   return e == cudaSuccess ? SPG_OK : SPG_ECUDA;
