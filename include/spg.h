@@ -184,7 +184,9 @@ spg_status sparse_decode_attention(const spg_params* p, const void* q, const voi
                                    const int32_t* sel, const int32_t* sel_cnt, float* out,
                                    float* lse, void* ws, size_t ws_bytes, spg_stream_t stream);
 
-/* sparse_page_select followed by sparse_decode_attention, one call. */
+/* sparse_page_select followed by sparse_decode_attention, one call; with page
+ * tables of at most 8192 pages both run in a single cluster launch (see
+ * sparse_decode_step). */
 spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const void* k_pool,
                                        const void* v_pool, const void* k_scale,
                                        const void* v_scale, const int32_t* page_table,
@@ -193,6 +195,20 @@ spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const
                                        const float* proj, int32_t* sel, int32_t* sel_cnt,
                                        float* out, float* lse, void* ws, size_t ws_bytes,
                                        spg_stream_t stream);
+
+/* The whole decode step in one call: the metadata update for the token just
+ * appended at seq_lens[b]-1 (as sparse_page_meta_update with rebuild == 0),
+ * then sparse_decode_select_attend.  Where the parameters allow it (page
+ * tables of at most 8192 pages), selection and attention run as one launch
+ * of one 8-CTA thread-block cluster per (batch, kv-head), and for the Quest
+ * selector with n_recent_pages >= 1 the append runs inside that launch too
+ * (the appended token's page is forced, so no scoring depends on it). */
+spg_status sparse_decode_step(const spg_params* p, const void* q, const void* k_pool,
+                              const void* v_pool, const void* k_scale, const void* v_scale,
+                              const int32_t* page_table, const int32_t* seq_lens, void* minmax,
+                              uint8_t* sketch, float* sketch_scale, const float* proj,
+                              int32_t* sel, int32_t* sel_cnt, float* out, float* lse, void* ws,
+                              size_t ws_bytes, spg_stream_t stream);
 
 /* Dense flash-decoding over every page of every sequence (the baseline the
  * Quest page compares against: the full KV read). */

@@ -88,6 +88,8 @@ def _load():
         "sparse_decode_select_attend": (
             [P, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
         "dense_decode_attention": ([P, v, v, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
+        "sparse_decode_step": (
+            [P, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
         "spg_read_device_error": ([v, POINTER(c_int32), v], c_int32),
         "spg_clear_device_error": ([v, v], c_int32),
     }
@@ -197,6 +199,17 @@ def sparse_decode_select_attend(p, q, k_pool, v_pool, k_scale, v_scale, page_tab
         _ptr(page_table), _ptr(seq_lens), _ptr(minmax), _ptr(sketch), _ptr(sketch_scale),
         _ptr(proj), _ptr(sel), _ptr(sel_cnt), _ptr(out), _ptr(lse), wp, wn, _stream(stream)),
         "sparse_decode_select_attend")
+
+
+def sparse_decode_step(p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+                       minmax=None, sketch=None, sketch_scale=None, proj=None, sel=None,
+                       sel_cnt=None, out=None, lse=None, ws=None, stream=None):
+    wp, wn = _ws(ws)
+    _check(LIB.sparse_decode_step(
+        ctypes.byref(p), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+        _ptr(page_table), _ptr(seq_lens), _ptr(minmax), _ptr(sketch), _ptr(sketch_scale),
+        _ptr(proj), _ptr(sel), _ptr(sel_cnt), _ptr(out), _ptr(lse), wp, wn, _stream(stream)),
+        "sparse_decode_step")
 
 
 def dense_decode_attention(p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens, out,

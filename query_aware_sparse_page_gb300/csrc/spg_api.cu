@@ -30,6 +30,7 @@ size_t workspace_bytes(const spg_params& p) {
   const size_t d = p.head_dim, MP = p.max_pages_per_seq;
   size_t off = 256;                                      // header: error word
   off += align256(sizeof(int32_t) * B * Hkv);            // split arrival counters
+  off += align256(sizeof(int32_t) * B * Hkv);            // scoring arrival counters
   off += align256(sizeof(float) * B * Hkv * MP);         // scores
   off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pm
   off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pl
@@ -45,6 +46,8 @@ Workspace carve_workspace(const spg_params& p, void* ws) {
   w.err = reinterpret_cast<int32_t*>(base);
   size_t off = 256;
   w.counters = reinterpret_cast<int32_t*>(base + off);
+  off += align256(sizeof(int32_t) * B * Hkv);
+  w.sel_counters = reinterpret_cast<int32_t*>(base + off);
   off += align256(sizeof(int32_t) * B * Hkv);
   w.scores = reinterpret_cast<float*>(base + off);
   off += align256(sizeof(float) * B * Hkv * MP);
@@ -80,6 +83,36 @@ spg_status check_meta_inputs(const spg_params* p, const void* minmax, const uint
   if (p->selector == SPG_SEL_SKETCH_INT4)
     return (ok_ptr(sketch) && ok_ptr(sketch_scale) && ok_ptr(proj)) ? SPG_OK : SPG_EINVAL;
   return SPG_EINVAL;  // SPG_SEL_ALL has no metadata and no selection
+}
+
+// select + attend: one cluster launch when the parameters allow it, else the
+// scoring/selection launch followed by the split-K attention launch.  With
+// append != 0 the fused launch also applies the Quest metadata append.
+cudaError_t select_attend(const spg_params& p, const void* q, const void* k_pool,
+                          const void* v_pool, const void* k_scale, const void* v_scale,
+                          const int32_t* page_table, const int32_t* seq_lens, void* minmax,
+                          const uint8_t* sketch, const float* sketch_scale, const float* proj,
+                          int32_t* sel, int32_t* sel_cnt, float* out, float* lse, int append,
+                          const Workspace& w, cudaStream_t st) {
+  if (spg::fused_supported(p, append)) {
+    const cudaError_t e = spg::launch_fused(p, q, k_pool, v_pool, k_scale, v_scale, page_table,
+                                            seq_lens, minmax, sketch, sketch_scale, proj, sel,
+                                            sel_cnt, out, lse, append, w, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  if (append) {
+    const cudaError_t e = spg::launch_meta_update(p, k_pool, k_scale, page_table, seq_lens, 0,
+                                                  minmax, const_cast<uint8_t*>(sketch),
+                                                  const_cast<float*>(sketch_scale), proj, w.err,
+                                                  st);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = spg::launch_select(p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
+                                     proj, w.scores, sel, sel_cnt, w, st);
+  if (e == cudaSuccess)
+    e = spg::launch_attention(p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens, sel,
+                              sel_cnt, out, lse, w, st);
+  return e;
 }
 
 spg_status check_kv(const spg_params* p, const void* k_pool, const void* v_pool,
@@ -175,9 +208,9 @@ spg_status sparse_page_score(const spg_params* p, const void* q, const int32_t* 
   if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
   if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
   const Workspace w = spg::carve_workspace(*p, ws);
-  return cuda_status(spg::launch_score(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
-                                       proj, scores, w.err,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(spg::launch_select(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
+                                        proj, scores, nullptr, nullptr, w,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 spg_status sparse_page_select(const spg_params* p, const void* q, const int32_t* page_table,
@@ -192,10 +225,8 @@ spg_status sparse_page_select(const spg_params* p, const void* q, const int32_t*
   if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
   const Workspace w = spg::carve_workspace(*p, ws);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = spg::launch_score(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
-                                    proj, w.scores, w.err, st);
-  if (e == cudaSuccess) e = spg::launch_topk(*p, w.scores, seq_lens, sel, sel_cnt, w.err, st);
-  return cuda_status(e);
+  return cuda_status(spg::launch_select(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
+                                        proj, w.scores, sel, sel_cnt, w, st));
 }
 
 spg_status sparse_decode_attention(const spg_params* p, const void* q, const void* k_pool,
@@ -235,12 +266,35 @@ spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const
   if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
   const Workspace w = spg::carve_workspace(*p, ws);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = spg::launch_score(*p, q, page_table, seq_lens, minmax, sketch, sketch_scale,
-                                    proj, w.scores, w.err, st);
-  if (e == cudaSuccess) e = spg::launch_topk(*p, w.scores, seq_lens, sel, sel_cnt, w.err, st);
+  return cuda_status(select_attend(*p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+                                   const_cast<void*>(minmax), sketch, sketch_scale, proj, sel,
+                                   sel_cnt, out, lse, 0, w, st));
+}
+
+spg_status sparse_decode_step(const spg_params* p, const void* q, const void* k_pool,
+                              const void* v_pool, const void* k_scale, const void* v_scale,
+                              const int32_t* page_table, const int32_t* seq_lens, void* minmax,
+                              uint8_t* sketch, float* sketch_scale, const float* proj,
+                              int32_t* sel, int32_t* sel_cnt, float* out, float* lse, void* ws,
+                              size_t ws_bytes, spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (!ok_ptr(q) || !ok_ptr(page_table) || !ok_ptr(seq_lens) || !ok_ptr(sel) ||
+      !ok_ptr(sel_cnt) || !ok_ptr(out) || (lse && !aligned16(lse)))
+    return SPG_EINVAL;
+  if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
+  if ((s = check_kv(p, k_pool, v_pool, k_scale, v_scale)) != SPG_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  int append_inside = spg::fused_supported(*p, 1) ? 1 : 0;
+  if (!append_inside)
+    e = spg::launch_meta_update(*p, k_pool, k_scale, page_table, seq_lens, 0, minmax, sketch,
+                                sketch_scale, proj, w.err, st);
   if (e == cudaSuccess)
-    e = spg::launch_attention(*p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens, sel,
-                              sel_cnt, out, lse, w, st);
+    e = select_attend(*p, q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens, minmax,
+                      sketch, sketch_scale, proj, sel, sel_cnt, out, lse, append_inside, w, st);
   return cuda_status(e);
 }
 

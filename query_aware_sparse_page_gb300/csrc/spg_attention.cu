@@ -1,4 +1,5 @@
-// Split-K flash-decoding over gathered KV pages, and the log-sum-exp combine.
+// Split-K flash-decoding over gathered KV pages, with the log-sum-exp merge
+// of the splits done by the last CTA of each unit.
 //
 // Sources: SALS长序列推理优化, SFAA (QK^T, online softmax, P@V, rescale over
 // the selected K/V; int8 K/V dequantised by their scales) and AICPU Tiling
@@ -6,19 +7,28 @@
 // Quest 完全拆解, 三段式 kernel (Approximate attention reads only the top-K
 // pages); Day 10·2 (softmax renormalised over the selected blocks only).
 //
-// Grid = (splits, batch * kv-heads).  A CTA owns a contiguous range of the
-// unit's page list (selected ids, or every page for the dense baseline).
-// All its threads first resolve the range's logical -> physical page ids
-// into shared memory (one round trip for the whole range), then each warp
-// runs its own pipeline over every W-th page of the range: lane 0 issues
-// cp.async.bulk copies (the TMA bulk engine) of the page's contiguous K and
-// V tiles ([S][d] per kv-head in the [P][Hkv][S][d] pool, plus the per-token
-// scales for int8) into a STAGES-deep shared-memory ring, completion tracked
-// by one mbarrier per stage; the warp computes on CUDA cores with the head
-// dimension split across lanes (a K/V row is read once, conflict-free) and
-// the G query rows of the kv-head group sharing every tile (GQA).  Every
-// barrier wait is bounded; a wait that runs out records SPG_DEVERR_TIMEOUT,
-// drains the copies this warp issued (bounded again) and stops.
+// Grid = (splits, batch * kv-heads), sized to one wave.  A CTA owns a
+// contiguous range of the unit's page list (selected ids, or every page for
+// the dense baseline) and is warp-specialised:
+//  * the producer warp resolves logical -> physical page ids 32 at a time
+//    (one lane per page), then lane 0 streams each page's contiguous K and V
+//    tiles ([S][d] of one kv-head in the [P][Hkv][S][d] pools, plus the
+//    per-token fp16 scales for int8) into a STAGES-deep shared-memory ring
+//    with cp.async.bulk (the TMA bulk-copy engine), one "full" mbarrier per
+//    stage carrying the byte count;
+//  * four consumer warps share every stage: each takes 4 tokens of each
+//    16-token round (8 lanes per token; 2 tokens and 16 lanes per token when
+//    the group has 4 or 8 query rows, to bound registers), computes the G
+//    query rows' logits on CUDA cores with a 3- or 4-step shuffle reduction,
+//    keeps a warp-wide running max per row and a per-lane accumulator for
+//    its token's channels, and releases the stage on an "empty" mbarrier
+//    (4 arrivals).
+// A lane's channels are 16-byte chunks lt, lt + LPT, ... of the row (or one
+// smaller piece), so the lanes of a token hit distinct bank groups and every
+// shared load runs at the minimum number of wavefronts.  Each of the G query
+// rows of the kv-head group reuses every staged tile (GQA).  All waits are
+// bounded; a wait that runs out records SPG_DEVERR_TIMEOUT and the CTA drains
+// (again bounded) the copies it issued before it leaves.
 //
 // Partials per (batch, q-head, split): running max m (log2 domain, scale
 // folded in), running sum l, unnormalised accumulator acc[d].  The last CTA
@@ -27,13 +37,13 @@
 // does the whole attention.
 #include <float.h>
 
-#include "spg_common.cuh"
+#include "spg_attn_core.cuh"
 #include "spg_internal.h"
 
 namespace spg {
 namespace {
 
-constexpr int kMaxPagesPerSplit = 1024;
+constexpr int kRingBytesTarget = 56 * 1024;
 
 struct AttnArgs {
   const void* q;
@@ -52,46 +62,41 @@ struct AttnArgs {
   float* out;
   float* lse;
   int32_t* err;
-  int Hkv, S, MP, n_phys, n_sel, pages_per_split;
+  int Hkv, S, MP, n_phys, n_sel, pages_per_split, stages;
   float scale_log2;
 };
 
-template <typename T>
-constexpr bool is_i8() { return sizeof(T) == 1; }
+template <typename T, typename TQ, int D, int G>
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_attn(const AttnArgs a) {
+  constexpr int CW = kConsumerWarps;
+  using Consumer = AttnConsumer<T, D, G>;
 
-// bytes of one stage: K tile, V tile, and for int8 the two fp16 scale rows
-template <typename T, int D>
-__host__ __device__ inline uint32_t stage_bytes(int S) {
-  const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
-  const uint32_t sc = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
-  return 2 * tile + 2 * sc;
-}
-
-template <typename T, int CPL>
-__device__ __forceinline__ void row_f32(const T* p, float* o) {
-  if constexpr (CPL == 4) load4_f32<T>(p, o);
-  else load2_f32<T>(p, o);
-}
-
-template <typename T, typename TQ, int D, int G, int W, int STAGES>
-__global__ void __launch_bounds__(W * 32) k_attn(const AttnArgs a) {
-  constexpr int CPL = D / 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = a.S;
+  const int STAGES = a.stages;
   const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
   const uint32_t scb = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
-  const uint32_t sbytes = stage_bytes<T, D>(S);
+  const uint32_t sbytes = kv_stage_bytes<T, D>(S);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(STAGES) * sbytes);
+  uint64_t* empty = full + kMaxStages;
+  int* s_nv = reinterpret_cast<int*>(empty + kMaxStages);
+  __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ring = smem + static_cast<size_t>(warp) * STAGES * sbytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * sbytes) +
-                   warp * STAGES;
-  int2* s_pg = reinterpret_cast<int2*>(smem + static_cast<size_t>(W) * STAGES * sbytes +
-                                       sizeof(uint64_t) * W * STAGES);
-
   const int unit = blockIdx.y, split = blockIdx.x;
   const int Hkv = a.Hkv;
   const int b = unit / Hkv, h = unit % Hkv;
+  const int Hq = Hkv * G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CW);
+    }
+    mbar_fence_init();
+  }
+  pdl_wait();  // sel / sel_cnt (and anything else) may come from the previous kernel
+
   int L = a.seq_lens[b];
   if (L < 0 || L > a.MP * S) {
     if (split == 0 && threadIdx.x == 0) record_error(a.err, SPG_DEVERR_SEQ_LEN);
@@ -107,193 +112,105 @@ __global__ void __launch_bounds__(W * 32) k_attn(const AttnArgs a) {
     }
   }
   const int s0 = split * a.pages_per_split;
-  const int s1 = min(s0 + a.pages_per_split, count);
-  const int n_range = max(s1 - s0, 0);
-
-  // resolve the range's pages: (physical page or -1, valid tokens)
-  for (int i = threadIdx.x; i < n_range; i += blockDim.x) {
-    const int idx = s0 + i;
-    int lp = a.sel ? a.sel[static_cast<size_t>(unit) * a.n_sel + idx] : idx;
-    int ph = -1, nv = 0;
-    if (lp < 0 || lp >= P) {
-      record_error(a.err, SPG_DEVERR_SEL);
-    } else {
-      ph = a.page_table[static_cast<size_t>(b) * a.MP + lp];
-      if (ph < 0 || ph >= a.n_phys) {
-        record_error(a.err, SPG_DEVERR_PAGE_ID);
-        ph = -1;
-      } else {
-        nv = min(S, L - lp * S);
-      }
-    }
-    s_pg[i] = make_int2(ph, nv);
-  }
-  if (lane == 0) {
-    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
-    mbar_fence_init();
-  }
+  const int n_range = max(min(s0 + a.pages_per_split, count) - s0, 0);
   __syncthreads();
 
-  // query rows of the group, pre-scaled into the log2 domain
-  const int Hq = Hkv * G;
-  const TQ* qb = static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D + lane * CPL;
-  float qf[G][CPL], acc[G][CPL], m[G], l[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    row_f32<TQ, CPL>(qb + g * D, qf[g]);
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      qf[g][c] *= a.scale_log2;
-      acc[g][c] = 0.f;
-    }
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-  }
+  Consumer cons;
 
-  const T* kpool = static_cast<const T*>(a.k_pool);
-  const T* vpool = static_cast<const T*>(a.v_pool);
-  const int nw = n_range > warp ? (n_range - warp + W - 1) / W : 0;
-  const uint64_t pol = policy_evict_first();
-
-  auto issue = [&](int j) {
-    const int stage = j % STAGES;
-    const int2 pg = s_pg[warp + W * j];
-    uint8_t* dst = ring + static_cast<size_t>(stage) * sbytes;
-    if (pg.x < 0) {
-      mbar_arrive_expect_tx(&bars[stage], 0);
-      return;
-    }
-    const size_t ph = static_cast<size_t>(pg.x) * Hkv + h;
-    mbar_arrive_expect_tx(&bars[stage], sbytes);
-    bulk_g2s_hint(dst, kpool + ph * S * D, tile, &bars[stage], pol);
-    bulk_g2s_hint(dst + tile, vpool + ph * S * D, tile, &bars[stage], pol);
-    if constexpr (is_i8<T>()) {
-      // per-token scale rows, S * 2 bytes (a multiple of 16 since S % 8 == 0)
-      bulk_g2s(dst + 2 * tile, a.k_scale + ph * S, scb, &bars[stage]);
-      bulk_g2s(dst + 2 * tile + scb, a.v_scale + ph * S, scb, &bars[stage]);
-    }
-  };
-
-  if (lane == 0)
-    for (int j = 0; j < min(STAGES, nw); ++j) issue(j);
-  __syncwarp();
-
-  bool timed_out = false;
-  for (int j = 0; j < nw; ++j) {
-    const int stage = j % STAGES;
-    const uint32_t parity = (j / STAGES) & 1;
-    if (!mbar_wait_bounded(&bars[stage], parity)) {
-      if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
-      // drain what this warp still has in flight, then stop
-      for (int jj = j; jj < min(j + STAGES, nw); ++jj)
-        mbar_wait_bounded(&bars[jj % STAGES], (jj / STAGES) & 1);
-      timed_out = true;
-      break;
-    }
-    const int2 pg = s_pg[warp + W * j];
-    if (pg.x >= 0) {
-      const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
-      const T* Ks = reinterpret_cast<const T*>(st);
-      const T* Vs = reinterpret_cast<const T*>(st + tile);
-      const __half* ksc = reinterpret_cast<const __half*>(st + 2 * tile);
-      const __half* vsc = reinterpret_cast<const __half*>(st + 2 * tile + scb);
-      const int nv = pg.y;
-      for (int t0 = 0; t0 < nv; t0 += 8) {
-        float z[8][G];
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const int t = t0 + tt;
-          if (t < nv) {
-            float kf[CPL];
-            row_f32<T, CPL>(Ks + t * D + lane * CPL, kf);
-            float ksv = 1.f;
-            if constexpr (is_i8<T>()) ksv = __half2float(ksc[t]);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float part = 0.f;
-#pragma unroll
-              for (int c = 0; c < CPL; ++c) part = fmaf(qf[g][c], kf[c], part);
-              z[tt][g] = warp_sum(part) * ksv;
-            }
+  if (warp == CW) {
+    // ---------------- producer: page ids, then bulk copies into the ring
+    const T* kpool = static_cast<const T*>(a.k_pool);
+    const T* vpool = static_cast<const T*>(a.v_pool);
+    const uint64_t pol = policy_evict_first();
+    int issued = 0;
+    bool ok = true;
+    for (int base = 0; base < n_range && ok; base += 32) {
+      int ph = -1, nv = 0;
+      const int j = base + lane;
+      if (j < n_range) {
+        const int idx = s0 + j;
+        const int lp = a.sel ? a.sel[static_cast<size_t>(unit) * a.n_sel + idx] : idx;
+        if (lp < 0 || lp >= P) {
+          record_error(a.err, SPG_DEVERR_SEL);
+        } else {
+          ph = a.page_table[static_cast<size_t>(b) * a.MP + lp];
+          if (ph < 0 || ph >= a.n_phys) {
+            record_error(a.err, SPG_DEVERR_PAGE_ID);
+            ph = -1;
           } else {
-#pragma unroll
-            for (int g = 0; g < G; ++g) z[tt][g] = -INFINITY;
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float cm = z[0][g];
-#pragma unroll
-          for (int tt = 1; tt < 8; ++tt) cm = fmaxf(cm, z[tt][g]);
-          const float mn = fmaxf(m[g], cm);  // finite: token t0 is valid
-          const float corr = exp2f(m[g] - mn);
-          l[g] *= corr;
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[g][c] *= corr;
-          m[g] = mn;
-#pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            const float pz = exp2f(z[tt][g] - mn);
-            l[g] += pz;
-            z[tt][g] = pz;  // reuse as the probability
-          }
-        }
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const int t = t0 + tt;
-          if (t < nv) {
-            float vf[CPL];
-            row_f32<T, CPL>(Vs + t * D + lane * CPL, vf);
-            float vsv = 1.f;
-            if constexpr (is_i8<T>()) vsv = __half2float(vsc[t]);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float pv = z[tt][g] * vsv;
-#pragma unroll
-              for (int c = 0; c < CPL; ++c) acc[g][c] = fmaf(pv, vf[c], acc[g][c]);
-            }
+            nv = min(S, L - lp * S);
           }
         }
       }
+      const int nb = min(32, n_range - base);
+      for (int jj = 0; jj < nb; ++jj) {
+        const int phj = __shfl_sync(0xffffffffu, ph, jj);
+        const int nvj = __shfl_sync(0xffffffffu, nv, jj);
+        const int k = base + jj;
+        const int stage = k % STAGES;
+        if (lane == 0) {
+          if (k >= STAGES && !mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1)) {
+            record_error(a.err, SPG_DEVERR_TIMEOUT);
+            ok = false;
+          }
+          if (ok) {
+            uint8_t* dst = smem + static_cast<size_t>(stage) * sbytes;
+            s_nv[stage] = phj >= 0 ? nvj : 0;
+            if (phj < 0) {
+              mbar_arrive_expect_tx(&full[stage], 0);
+            } else {
+              const size_t row = static_cast<size_t>(phj) * Hkv + h;
+              mbar_arrive_expect_tx(&full[stage], sbytes);
+              bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
+              bulk_g2s_hint(dst + tile, vpool + row * S * D, tile, &full[stage], pol);
+              if constexpr (is_i8<T>()) {
+                bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
+                bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
+              }
+            }
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
     }
-    __syncwarp();
-    if (lane == 0 && j + STAGES < nw) {
-      fence_proxy_async();
-      issue(j + STAGES);
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (!ok && lane == 0) {
+      // drain the copies still in flight before the CTA can leave
+      for (int k = max(0, issued - STAGES); k < issued; ++k)
+        mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
     }
-    __syncwarp();
+  } else {
+    // ---------------- consumers
+    cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
+              a.scale_log2, warp, lane);
+    for (int k = 0; k < n_range; ++k) {
+      const int stage = k % STAGES;
+      if (!mbar_wait_bounded(&full[stage], (k / STAGES) & 1)) {
+        if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
+        break;
+      }
+      const int nv = s_nv[stage];
+      if (nv > 0) cons.consume(smem + static_cast<size_t>(stage) * sbytes, S, nv);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    cons.fold();
   }
-  (void)timed_out;
 
-  // merge the W warps of this CTA (reusing the ring), then write the partial
+  pdl_trigger();
+  // merge the consumer warps of this CTA (reusing the ring), write the partial
   __syncthreads();
-  float* s_m = reinterpret_cast<float*>(smem);          // [W][G]
-  float* s_l = s_m + W * G;                              // [W][G]
-  float* s_acc = s_l + W * G;                            // [W][G][D]
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (lane == 0) {
-      s_m[warp * G + g] = m[g];
-      s_l[warp * G + g] = l[g];
-    }
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) s_acc[(warp * G + g) * D + lane * CPL + c] = acc[g][c];
-  }
+  float* s_m = reinterpret_cast<float*>(smem);  // [CW][G]
+  float* s_l = s_m + CW * G;                     // [CW][G]
+  float* s_acc = s_l + CW * G;                   // [CW][G][D]
+  if (warp < CW) cons.store(s_m, s_l, s_acc, lane);
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D, c = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, s_m[w * G + g]);
-    float A = 0.f, Ls = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float f = exp2f(s_m[w * G + g] - M);
-        A = fmaf(s_acc[(w * G + g) * D + c], f, A);
-        Ls = fmaf(s_l[w * G + g], f, Ls);
-      }
-    }
+    float M, Ls, A;
+    lse_merge(s_m, s_l, s_acc, CW, G, D, g, c, M, Ls, A);
     const size_t row = static_cast<size_t>(b) * Hq + h * G + g;
     const size_t pidx = row * kMaxSplits + split;
     a.pacc[pidx * D + c] = A;
@@ -309,7 +226,6 @@ __global__ void __launch_bounds__(W * 32) k_attn(const AttnArgs a) {
   // counting themselves in; no CTA ever waits for another.
   __threadfence();
   __syncthreads();
-  __shared__ int s_last;
   if (threadIdx.x == 0) {
     const int prev = atomicAdd(&a.counters[unit], 1);
     s_last = (prev == static_cast<int>(gridDim.x) - 1);
@@ -318,31 +234,44 @@ __global__ void __launch_bounds__(W * 32) k_attn(const AttnArgs a) {
   if (!s_last) return;
   __threadfence();
   const int n_split = gridDim.x;
-  for (int g = warp; g < G; g += W) {
+  // weights of every split per row, in shared memory (reusing the ring)
+  float* s_w = reinterpret_cast<float*>(smem);  // [G][n_split]
+  float* s_M = s_w + G * kMaxSplits;            // [G]
+  float* s_L = s_M + G;                         // [G]
+  for (int g = warp; g < G; g += CW + 1) {
     const size_t row = static_cast<size_t>(b) * Hq + h * G + g;
     const float* pmr = a.pm + row * kMaxSplits;
     const float* plr = a.pl + row * kMaxSplits;
     float M = -INFINITY;
     for (int sp = lane; sp < n_split; sp += 32) M = fmaxf(M, __ldcg(pmr + sp));
     M = warp_max(M);
-    float o[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) o[c] = 0.f;
     float Ls = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < n_split; ++sp) {
-        const float f = exp2f(__ldcg(pmr + sp) - M);
-        Ls = fmaf(__ldcg(plr + sp), f, Ls);
-        const float* A = a.pacc + (row * kMaxSplits + sp) * D + lane * CPL;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) o[c] = fmaf(__ldcg(A + c), f, o[c]);
-      }
+    for (int sp = lane; sp < n_split; sp += 32) {
+      const float f = M == -INFINITY ? 0.f : exp2f(__ldcg(pmr + sp) - M);
+      s_w[g * kMaxSplits + sp] = f;
+      Ls = fmaf(__ldcg(plr + sp), f, Ls);
     }
-    float* orow = a.out + row * D + lane * CPL;
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) orow[c] = o[c] * inv;
-    if (a.lse && lane == 0) a.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    Ls = warp_sum(Ls);
+    if (lane == 0) {
+      s_M[g] = M;
+      s_L[g] = Ls;
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D, c = idx % D;
+    const size_t row = static_cast<size_t>(b) * Hq + h * G + g;
+    const float* A = a.pacc + row * kMaxSplits * D + c;
+    float o0 = 0.f, o1 = 0.f;
+    int sp = 0;
+    for (; sp + 1 < n_split; sp += 2) {
+      o0 = fmaf(__ldcg(A + sp * D), s_w[g * kMaxSplits + sp], o0);
+      o1 = fmaf(__ldcg(A + (sp + 1) * D), s_w[g * kMaxSplits + sp + 1], o1);
+    }
+    if (sp < n_split) o0 = fmaf(__ldcg(A + sp * D), s_w[g * kMaxSplits + sp], o0);
+    const float Ls = s_L[g];
+    a.out[row * D + c] = Ls > 0.f ? (o0 + o1) / Ls : 0.f;
+    if (c == 0 && a.lse) a.lse[row] = Ls > 0.f ? (s_M[g] + log2f(Ls)) * kLn2 : -INFINITY;
   }
   if (threadIdx.x == 0) a.counters[unit] = 0;  // ready for the next call
 }
@@ -350,37 +279,40 @@ __global__ void __launch_bounds__(W * 32) k_attn(const AttnArgs a) {
 template <typename T, typename TQ, int D, int G>
 cudaError_t attn_typed(const spg_params& p, const AttnArgs& a0, int pages_upper, float* out,
                        float* lse, cudaStream_t st) {
-  constexpr int W = 4;
-  constexpr int STAGES = is_i8<T>() ? 2 : 3;
+  constexpr int threads = (kConsumerWarps + 1) * 32;
   AttnArgs a = a0;
   const int units = p.batch * p.num_kv_heads;
-  const uint32_t sb = stage_bytes<T, D>(p.page_size);
-  auto kern = k_attn<T, TQ, D, G, W, STAGES>;
-  const size_t ring = static_cast<size_t>(W) * STAGES * sb;
-  const size_t merge = sizeof(float) * W * G * (D + 2);
-  // split plan: about two CTAs per SM in total, bounded by the workspace
-  const int ctas_per_sm = 2;
-  const int target = device_sm_count() * ctas_per_sm;
-  int n_split = (target + units - 1) / units;
-  n_split = max(1, min(n_split, min(kMaxSplits, max(pages_upper, 1))));
-  int pps = (max(pages_upper, 1) + n_split - 1) / n_split;
-  pps = max(pps, (pages_upper + kMaxSplits - 1) / kMaxSplits);
-  if (pps > kMaxPagesPerSplit) return cudaErrorInvalidValue;
-  n_split = max(1, (pages_upper + pps - 1) / pps);
-  a.pages_per_split = pps;
-  const size_t smem = max(ring + sizeof(uint64_t) * W * STAGES + sizeof(int2) * pps, merge);
-  static int configured = 0;
-  if (smem > 48 * 1024 && static_cast<int>(smem) > configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = static_cast<int>(smem);
+  const uint32_t sb = kv_stage_bytes<T, D>(p.page_size);
+  const int stages = max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb)));
+  a.stages = stages;
+  auto kern = k_attn<T, TQ, D, G>;
+  const size_t ring = static_cast<size_t>(stages) * sb;
+  const size_t bars = sizeof(uint64_t) * 2 * kMaxStages + sizeof(int) * kMaxStages;
+  const size_t merge = sizeof(float) * kConsumerWarps * G * (D + 2);
+  const size_t comb = sizeof(float) * (G * kMaxSplits + 2 * G);
+  const size_t smem = max(ring + bars, max(merge, comb));
+  cudaError_t e = ensure_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  // one wave: as many CTAs as fit on the GPU at once, spread over the units
+  static int per_sm_cache[2] = {0, 0};  // (smem bytes, CTAs per SM) of the last query
+  int per_sm = per_sm_cache[0] == static_cast<int>(smem) ? per_sm_cache[1] : 0;
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    per_sm_cache[0] = static_cast<int>(smem);
+    per_sm_cache[1] = per_sm;
   }
+  const int slots = device_sm_count() * per_sm;
+  int n_split = max(1, slots / units);
+  n_split = min(n_split, min(kMaxSplits, max(pages_upper, 1)));
+  const int pps = (max(pages_upper, 1) + n_split - 1) / n_split;
+  n_split = max(1, (max(pages_upper, 1) + pps - 1) / pps);
+  a.pages_per_split = pps;
   a.out = out;
   a.lse = lse;
-  dim3 grid(n_split, units);
-  kern<<<grid, W * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(n_split, units), dim3(threads), smem, st, a);
 }
 
 template <typename T, typename TQ>

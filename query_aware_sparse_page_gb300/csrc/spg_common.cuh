@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+#include <utility>
+
 #include "spg.h"
 
 namespace spg {
@@ -47,6 +50,38 @@ __device__ __forceinline__ void load4_f32<int8_t>(const int8_t* p, float* o) {
   o[1] = static_cast<float>(static_cast<int8_t>((r >> 8) & 0xff));
   o[2] = static_cast<float>(static_cast<int8_t>((r >> 16) & 0xff));
   o[3] = static_cast<float>(static_cast<int8_t>(r >> 24));
+}
+
+// N consecutive elements (N * sizeof(T) in {4, 8, 16} bytes, aligned) -> fp32
+template <typename T, int N>
+__device__ __forceinline__ void load_cvt(const T* p, float* o) {
+  constexpr int BYTES = N * static_cast<int>(sizeof(T));
+  static_assert(BYTES == 4 || BYTES == 8 || BYTES == 16, "4, 8 or 16 bytes");
+  uint32_t w[BYTES / 4];
+  if constexpr (BYTES == 16) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+  } else if constexpr (BYTES == 8) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    w[0] = r.x; w[1] = r.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+#pragma unroll
+  for (int i = 0; i < BYTES / 4; ++i) {
+    if constexpr (sizeof(T) == 1) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[4 * i + j] = static_cast<float>(static_cast<int8_t>((w[i] >> (8 * j)) & 0xffu));
+    } else if constexpr (std::is_same<T, __half>::value) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      o[2 * i] = f.x;
+      o[2 * i + 1] = f.y;
+    } else {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
 }
 
 // 2 consecutive elements -> fp32
@@ -97,6 +132,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -141,6 +180,88 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
       "[%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
+}
+
+// adds `bytes` to the transaction count the barrier's current phase waits for
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// ---- thread-block clusters and distributed shared memory ---------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory accesses
+// (local and remote) before it with those after it
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// shared::cluster address of `p` (a shared variable) in CTA `rank`
+__device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+// Kernels are launched with programmatic stream serialisation: a kernel may be
+// scheduled while its predecessor drains, runs its prologue, and waits here
+// before it reads anything a predecessor may have written.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// lets the next kernel in the stream start its prologue
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit when it needs more than the
+// default 48 KB (once per kernel and size; repeated calls are no-ops).
+template <typename... KArgs>
+inline cudaError_t ensure_smem(void (*kern)(KArgs...), size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  struct Entry {
+    const void* fn;
+    size_t bytes;
+  };
+  static Entry cache[64];
+  static int n = 0;
+  const void* fn = reinterpret_cast<const void*>(kern);
+  for (int i = 0; i < n; ++i)
+    if (cache[i].fn == fn && cache[i].bytes >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && n < 64) cache[n++] = Entry{fn, bytes};
+  return e;
 }
 
 // order-preserving map of an fp32 score to uint32 (larger float -> larger key)

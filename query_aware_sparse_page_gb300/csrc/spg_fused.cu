@@ -1,0 +1,619 @@
+// The whole decode step in one launch: metadata append (Quest), page scoring,
+// exact top-k, sparse flash-decoding and the log-sum-exp merge, with one
+// thread-block cluster of 8 CTAs per (batch, kv-head) unit.
+//
+// Sources: Quest 完全拆解 (关键性估计算法: insert-time min/max, 核心机制: the
+// per-page bound, 三段式 kernel: estimate -> top-k -> approximate attention);
+// SALS长序列推理优化 (QSI scoring and exact top-k, SFAA attention, AICPU
+// Tiling challenge 2: a row split across cores merged by a reduction);
+// SequenceO1 close reading §2.4 / §3.3 (fusing selection and attention: the
+// indices never leave the chip here, they cross shared memory).
+//
+// Phases of one cluster (every CTA has 4 consumer warps and 1 producer warp):
+//  1. scan: the unit's candidate pages are split into 8 contiguous chunks.
+//     The producer resolves page ids (one lane per page) and streams the
+//     metadata rows of its chunk (Quest: m and M, 2*d elements; sketch: the
+//     block's int4 codes) into the shared-memory ring with cp.async.bulk,
+//     several rows per stage; the consumers score each row and store its
+//     order-preserving key straight into the leader CTA's shared memory
+//     (distributed shared memory, st.shared::cluster).
+//  2. cluster barrier; the leader (rank 0) runs the exact top-k over the
+//     keys, adds the forced pages and writes sel / sel_cnt; cluster barrier.
+//  3. attend: each CTA takes a contiguous slice of the selection (read from
+//     the leader's shared memory), streams those pages' K/V tiles through the
+//     same ring (TMA bulk copies, page-table lookup by the producer) and runs
+//     the online-softmax consumer; the CTA's partial (m, l, acc) per query row
+//     goes into the leader's shared memory.
+//  4. cluster barrier; the leader merges the 8 partials and writes out / lse.
+// No CTA waits on another except at the three hardware cluster barriers,
+// which every thread of every CTA reaches on every path; all mbarrier waits
+// are bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still
+// reaches the cluster barriers.
+#include "spg_attn_core.cuh"
+#include "spg_internal.h"
+#include "spg_select_core.cuh"
+
+namespace spg {
+namespace {
+
+constexpr int kMaxCluster = 8;
+constexpr int kMaxScanRows = 64;
+constexpr int kMaxPagesPerStage = 8;
+constexpr int kFusedMaxPages = 8192;  // candidate keys the leader holds
+// A stage carries several pages (or metadata rows): the handshake of a ring
+// stage costs about the same whatever its size, so ~16 KB stages and a
+// 64 KB ring per CTA (two CTAs per SM) keep HBM busy where one page per
+// stage would not.
+constexpr int kStageBytesTarget = 16 * 1024;
+constexpr int kRingBytesTarget = 64 * 1024;
+
+struct FusedArgs {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const __half* k_scale;
+  const __half* v_scale;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  void* minmax;  // written only by the append
+  const uint8_t* sketch;
+  const float* sketch_scale;
+  const float* proj;
+  int32_t* sel;
+  int32_t* sel_cnt;
+  float* out;
+  float* lse;
+  int32_t* err;
+  int Hkv, S, MP, n_phys, n_sink, n_recent, n_sel, stages, rows_per_stage, append;
+  int cluster, pages_per_stage;
+  uint32_t stage_bytes, row_bytes, page_bytes, ring_bytes, keys_off, sel_off;
+  float scale_log2, inv_sqrt_d;
+};
+
+// consumer-only barrier (named barrier 1, the 4 consumer warps)
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+template <typename T, int CPL>
+__device__ __forceinline__ void smem_chunk(const uint8_t* p, uint32_t (&w)[CPL / 2]) {
+  if constexpr (CPL == 8) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+  } else {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    w[0] = r.x; w[1] = r.y;
+  }
+}
+
+// Quest append of the token at L-1 for (b, h) by one warp (Quest 完全拆解,
+// 关键性估计算法); the page's first token starts its statistics.
+template <typename T, int D>
+__device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int lane) {
+  constexpr int CPL = D / 32;
+  const int S = a.S, t = L - 1, p = t / S, slot = t % S;
+  const int phys = a.page_table[static_cast<size_t>(b) * a.MP + p];
+  if (phys < 0 || phys >= a.n_phys) {
+    if (lane == 0) record_error(a.err, SPG_DEVERR_PAGE_ID);
+    return;
+  }
+  const size_t ph = static_cast<size_t>(phys) * a.Hkv + h;
+  const T* k = static_cast<const T*>(a.k_pool) + (ph * S + slot) * D + lane * CPL;
+  T* lo = static_cast<T*>(a.minmax) + ph * 2 * D + lane * CPL;
+  T* hi = lo + D;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const T kv = k[c];
+    if (slot == 0) {
+      lo[c] = kv;
+      hi[c] = kv;
+    } else {
+      const float kf = to_f32(kv);
+      if (kf < to_f32(lo[c])) lo[c] = kv;
+      if (kf > to_f32(hi[c])) hi[c] = kv;
+    }
+  }
+}
+
+template <typename T, typename TQ, int D, int G, int SEL>
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const FusedArgs a) {
+  constexpr int CW = kConsumerWarps;
+  const int C = a.cluster;
+  constexpr int QCPL = D / 16;  // Quest scan: channels per lane of a half-warp
+  using Consumer = AttnConsumer<T, D, G>;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_qbar[SEL ? 256 : 1];
+  __shared__ float s_P[SEL ? 256 * 16 : 1];
+  __shared__ int s_qc[4];
+  __shared__ float s_sq;
+  __shared__ int s_count;
+
+  const int S = a.S, STAGES = a.stages, R = a.rows_per_stage, PPS = a.pages_per_stage;
+  const uint32_t sbytes = a.stage_bytes, rb = a.row_bytes, pbytes = a.page_bytes;
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.ring_bytes);
+  uint64_t* empty = full + kMaxStages;
+  int* s_np = reinterpret_cast<int*>(empty + kMaxStages);                // [stages] pages in stage
+  int* s_nv = s_np + kMaxStages;                                          // [stages][8] valid tokens
+  int* s_rows = s_nv + kMaxStages * kMaxPagesPerStage;                    // [stages][64] scan rows
+  float* s_rsc = reinterpret_cast<float*>(s_rows + kMaxStages * kMaxScanRows);  // [stages][64]
+  uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + a.keys_off);       // leader: keys
+  float* s_part = reinterpret_cast<float*>(smem + a.keys_off);            // leader: partials
+  int* s_sel = reinterpret_cast<int*>(smem + a.sel_off);                  // leader: selection
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int unit = blockIdx.y;
+  const int Hkv = a.Hkv, b = unit / Hkv, h = unit % Hkv, Hq = Hkv * G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CW);
+    }
+    mbar_fence_init();
+  }
+  pdl_wait();
+  int L = a.seq_lens[b];
+  if (L < 0 || L > a.MP * S) {
+    if (rank == 0 && threadIdx.x == 0) record_error(a.err, SPG_DEVERR_SEQ_LEN);
+    L = 0;
+  }
+  const int P = (L + S - 1) / S;
+  const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo), nc = hi - lo;
+  __syncthreads();
+
+  if constexpr (SEL == 0) {
+    // the appended token's page is forced (n_recent >= 1): no CTA scans it
+    if (a.append && rank == C - 1 && warp == 0 && L > 0) append_minmax_warp<T, D>(a, b, h, L, lane);
+  }
+
+  // ------------------------------------------------------------------ scan
+  const int cpc = (nc + C - 1) / C;
+  const int c0 = lo + min(nc, static_cast<int>(rank) * cpc);
+  const int rows = lo + min(nc, static_cast<int>(rank + 1) * cpc) - c0;
+  const int n_scan = (rows + R - 1) / R;
+  const uint32_t keys_leader = map_rank(s_keys, 0);
+  bool ok = true;
+
+  if (warp == CW) {
+    // producer: one lane per row, so a batch of 32 rows is issued at once;
+    // the next batch's page ids are in flight while this one is issued
+    auto resolve = [&](int base, int& ph, float& sc) {
+      const int j = base + lane;
+      ph = -1;
+      sc = 0.f;
+      if (j < rows) {
+        ph = a.page_table[static_cast<size_t>(b) * a.MP + c0 + j];
+        if (ph < 0 || ph >= a.n_phys) {
+          record_error(a.err, SPG_DEVERR_PAGE_ID);
+          ph = -1;
+        } else if constexpr (SEL == 1) {
+          sc = __ldg(a.sketch_scale + static_cast<size_t>(ph) * Hkv + h);
+        }
+      }
+    };
+    int ph_cur, ph_nxt = -1;
+    float sc_cur, sc_nxt = 0.f;
+    resolve(0, ph_cur, sc_cur);
+    for (int base = 0; base < rows; base += 32) {
+      if (base + 32 < rows) resolve(base + 32, ph_nxt, sc_nxt);
+      const int i = base + lane, r = i % R, k = i / R, stage = k % STAGES;
+      const bool mine = i < rows;
+      // the lane holding a stage's first row waits until the slot is free
+      // (a batch spans at most STAGES stages, so every wait is one phase ahead)
+      bool lok = true;
+      if (mine && r == 0 && k >= STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
+      if (!lok) record_error(a.err, SPG_DEVERR_TIMEOUT);
+      ok = __all_sync(0xffffffffu, lok) != 0;
+      if (!ok) break;
+      if (mine) {
+        s_rows[stage * kMaxScanRows + r] = ph_cur >= 0 ? c0 + i : -(c0 + i) - 1;
+        s_rsc[stage * kMaxScanRows + r] = sc_cur;
+        if (ph_cur >= 0) {
+          const uint8_t* src;
+          if constexpr (SEL == 0)
+            src = static_cast<const uint8_t*>(a.minmax) +
+                  (static_cast<size_t>(ph_cur) * Hkv + h) * 2 * D * sizeof(T);
+          else
+            src = a.sketch + (static_cast<size_t>(ph_cur) * Hkv + h) * S * 8;
+          mbar_expect_tx(&full[stage], rb);
+          bulk_g2s(ring + static_cast<size_t>(stage) * sbytes + r * rb, src, rb, &full[stage]);
+        }
+      }
+      __syncwarp();
+      // the lane holding a stage's last row closes it (after every expect_tx)
+      if (mine && (r == R - 1 || i == rows - 1)) mbar_arrive(&full[stage]);
+      ph_cur = ph_nxt;
+      sc_cur = sc_nxt;
+    }
+  } else {
+    // consumers
+    if constexpr (SEL == 0) {
+      float qf[G][QCPL];
+      const int hl = lane & 15, hwid = warp * 2 + (lane >> 4);
+      quest_query<T, D, G>(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
+                           hl, qf);
+      for (int ks = 0; ks < n_scan; ++ks) {
+        const int stage = ks % STAGES;
+        if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
+          if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const int nr = min(R, rows - ks * R);
+        const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
+        for (int r = hwid; r < R; r += 2 * CW) {  // R is a multiple of 8: both halves iterate together
+          const int enc = r < nr ? s_rows[stage * kMaxScanRows + r] : -1;
+          uint32_t wm[QCPL / 2], wM[QCPL / 2];
+          if (r < nr && enc >= 0) {
+            smem_chunk<T, QCPL>(st + r * rb + hl * QCPL * sizeof(T), wm);
+            smem_chunk<T, QCPL>(st + r * rb + (D + hl * QCPL) * sizeof(T), wM);
+          } else {
+#pragma unroll
+            for (int c = 0; c < QCPL / 2; ++c) wm[c] = wM[c] = 0u;
+          }
+          const float score = quest_bound<T, D, G>(qf, wm, wM);
+          if (r < nr && hl == 0) {
+            const int p = enc >= 0 ? enc : -enc - 1;
+            st_cluster_u32(keys_leader + 4u * (p - lo), score_key(enc >= 0 ? score : -INFINITY));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+      }
+    } else {
+      // index query of the group, built by the consumer warps only
+      const TQ* qb = static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D;
+      constexpr int DS = 16;
+      for (int i = threadIdx.x; i < D; i += CW * 32) {
+        float s = to_f32(qb[i]);
+        for (int g = 1; g < G; ++g) s = __fadd_rn(s, to_f32(qb[g * D + i]));
+        s_qbar[i] = __fdiv_rn(s, static_cast<float>(G));
+      }
+      for (int i = threadIdx.x; i < D * DS; i += CW * 32) s_P[i] = a.proj[i];
+      consumers_sync();
+      if (warp == 0) {
+        float qt = 0.f;
+        if (lane < DS)
+          for (int i = 0; i < D; ++i) qt = __fadd_rn(qt, __fmul_rn(s_qbar[i], s_P[i * DS + lane]));
+        float am = fabsf(qt);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const float sq = am > 0.f ? __fdiv_rn(am, 127.0f) : 1.0f;
+        const int qc = max(-127, min(127, static_cast<int>(rintf(__fdiv_rn(qt, sq)))));
+        int c[DS];
+#pragma unroll
+        for (int j = 0; j < DS; ++j) c[j] = __shfl_sync(0xffffffffu, qc, j);
+        if (lane == 0) {
+          s_qc[0] = pack_i8x4(c[0], c[2], c[4], c[6]);
+          s_qc[1] = pack_i8x4(c[1], c[3], c[5], c[7]);
+          s_qc[2] = pack_i8x4(c[8], c[10], c[12], c[14]);
+          s_qc[3] = pack_i8x4(c[9], c[11], c[13], c[15]);
+          s_sq = sq;
+        }
+      }
+      consumers_sync();
+      const int qc[4] = {s_qc[0], s_qc[1], s_qc[2], s_qc[3]};
+      const float sq = s_sq;
+      for (int ks = 0; ks < n_scan; ++ks) {
+        const int stage = ks % STAGES;
+        if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
+          if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const int nr = min(R, rows - ks * R);
+        const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
+        for (int r = warp; r < nr; r += CW) {  // one warp per block
+          const int enc = s_rows[stage * kMaxScanRows + r];
+          float score = -INFINITY;
+          if (enc >= 0) {
+            uint2 wk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (lane + 32 * k < S)
+                wk[k] = *reinterpret_cast<const uint2*>(st + r * rb + (lane + 32 * k) * 8);
+            const float cz =
+                __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r]), a.inv_sqrt_d);
+            score = sketch_block_score(wk, S, qc, cz);
+          }
+          if (lane == 0) {
+            const int p = enc >= 0 ? enc : -enc - 1;
+            st_cluster_u32(keys_leader + 4u * (p - lo), score_key(score));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+      }
+    }
+  }
+  cluster_sync();  // every key is in the leader
+
+  // ------------------------------------------------------------- selection
+  if (rank == 0) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int nf = P - nc;
+    const int k_top = min(max(a.n_sel - nf, 0), nc);
+    for (int i = tid; i < lo; i += nt) s_sel[i] = i;
+    for (int j = tid; j < P - hi; j += nt) s_sel[lo + k_top + j] = hi + j;
+    const int count = lo + k_top + (P - hi);
+    if (k_top == nc) {
+      for (int i = tid; i < nc; i += nt) s_sel[lo + i] = lo + i;
+    } else if (k_top > 0) {
+      block_topk(s_keys, nc, k_top, lo, s_sel + lo, *reinterpret_cast<TopkShared*>(ring));
+    }
+    if (tid == 0) s_count = count;
+    __syncthreads();
+    int32_t* gsel = a.sel + static_cast<size_t>(unit) * a.n_sel;
+    for (int i = tid; i < a.n_sel; i += nt) gsel[i] = i < count ? s_sel[i] : -1;
+    if (tid == 0) a.sel_cnt[unit] = count;
+  }
+  cluster_sync();  // the selection is in the leader
+
+  // ---------------------------------------------------------------- attend
+  const int count = ld_cluster_s32(map_rank(&s_count, 0));
+  const int ppc = (count + C - 1) / C;
+  const int a0 = min(count, static_cast<int>(rank) * ppc);
+  const int n_att = min(count, a0 + ppc) - a0;
+  Consumer cons;
+  if (warp == CW) {
+    const uint32_t sel_leader = map_rank(s_sel, 0);
+    const T* kpool = static_cast<const T*>(a.k_pool);
+    const T* vpool = static_cast<const T*>(a.v_pool);
+    const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
+    const uint32_t scb = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
+    const uint64_t pol = policy_evict_first();
+    for (int base = 0; base < n_att && ok; base += 32) {
+      int ph = -1, nv = 0;
+      const int j = base + lane;
+      if (j < n_att) {
+        const int lp = ld_cluster_s32(sel_leader + 4u * (a0 + j));
+        if (lp < 0 || lp >= P) {
+          record_error(a.err, SPG_DEVERR_SEL);
+        } else {
+          ph = a.page_table[static_cast<size_t>(b) * a.MP + lp];
+          if (ph < 0 || ph >= a.n_phys) {
+            record_error(a.err, SPG_DEVERR_PAGE_ID);
+            ph = -1;
+          } else {
+            nv = min(S, L - lp * S);
+          }
+        }
+      }
+      // one stage at a time: PPS pages, one lane each
+      const int nb = min(32, n_att - base);
+      for (int s0 = 0; s0 < nb && ok; s0 += PPS) {
+        const int k = n_scan + (base + s0) / PPS, stage = k % STAGES;
+        bool lok = true;
+        if (lane == 0 && k >= STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
+        if (!lok) record_error(a.err, SPG_DEVERR_TIMEOUT);
+        ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const int np = min(PPS, nb - s0);
+        if (lane >= s0 && lane < s0 + np) {
+          const int i = lane - s0;
+          uint8_t* dst = ring + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes;
+          s_nv[stage * kMaxPagesPerStage + i] = ph >= 0 ? nv : 0;
+          if (ph >= 0) {
+            const size_t row = static_cast<size_t>(ph) * Hkv + h;
+            mbar_expect_tx(&full[stage], 2 * tile + 2 * scb);
+            bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
+            bulk_g2s_hint(dst + tile, vpool + row * S * D, tile, &full[stage], pol);
+            if constexpr (is_i8<T>()) {
+              bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
+              bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
+            }
+          }
+        }
+        if (lane == 0) s_np[stage] = np;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+      }
+    }
+    if (!ok && lane == 0) {
+      // drain the copies this producer may still have in flight before the ring is reused
+      // (bounded waits; uses that were never issued simply time out)
+      const int issued = n_scan + (n_att + PPS - 1) / PPS;
+      for (int k = max(0, issued - STAGES); k < issued; ++k)
+        mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
+    }
+  } else {
+    cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
+              a.scale_log2, warp, lane);
+    const int n_att_st = (n_att + PPS - 1) / PPS;
+    for (int ka = 0; ka < n_att_st && ok; ++ka) {
+      const int k = n_scan + ka, stage = k % STAGES;
+      if (!mbar_wait_bounded(&full[stage], (k / STAGES) & 1)) {
+        if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
+        break;
+      }
+      const int np = s_np[stage];
+      for (int i = 0; i < np; ++i) {
+        const int nv = s_nv[stage * kMaxPagesPerStage + i];
+        if (nv > 0)
+          cons.consume(ring + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes, S,
+                       nv);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    cons.fold();
+  }
+  pdl_trigger();
+
+  // the CTA's partial (merge of its consumer warps) into the leader
+  __syncthreads();
+  float* s_m = reinterpret_cast<float*>(ring);  // [CW][G]
+  float* s_l = s_m + CW * G;
+  float* s_acc = s_l + CW * G;                   // [CW][G][D]
+  if (warp < CW) cons.store(s_m, s_l, s_acc, lane);
+  __syncthreads();
+  const uint32_t part_leader = map_rank(s_part, 0);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D, c = idx % D;
+    float M, Ls, A;
+    lse_merge(s_m, s_l, s_acc, CW, G, D, g, c, M, Ls, A);
+    // leader layout: m [C][G], l [C][G], acc [C][G][D]
+    st_cluster_f32(part_leader + 4u * (C * G + C * G + (rank * G + g) * D + c), A);
+    if (c == 0) {
+      st_cluster_f32(part_leader + 4u * (rank * G + g), M);
+      st_cluster_f32(part_leader + 4u * (C * G + rank * G + g), Ls);
+    }
+  }
+  cluster_sync();  // every partial is in the leader
+
+  if (rank == 0) {
+    const float* pm = s_part;
+    const float* pl = s_part + C * G;
+    const float* pa = s_part + 2 * C * G;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+      const int g = idx / D, c = idx % D;
+      float M, Ls, A;
+      lse_merge(pm, pl, pa, C, G, D, g, c, M, Ls, A);
+      const size_t row = static_cast<size_t>(b) * Hq + h * G + g;
+      a.out[row * D + c] = Ls > 0.f ? A / Ls : 0.f;
+      if (c == 0 && a.lse) a.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    }
+  }
+}
+
+template <typename T, typename TQ, int D, int G>
+cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
+  constexpr int threads = (kConsumerWarps + 1) * 32;
+  const int S = p.page_size;
+  const uint32_t pb = kv_stage_bytes<T, D>(S);
+  const uint32_t rb = p.selector == SPG_SEL_QUEST ? 2u * D * sizeof(T) : static_cast<uint32_t>(S) * 8u;
+  int pps = 1;
+  while (pps * 2 <= kMaxPagesPerStage && (pps * 2) * pb <= static_cast<uint32_t>(kStageBytesTarget))
+    pps *= 2;
+  int R = static_cast<int>(std::max<uint32_t>(pps * pb, kStageBytesTarget) / rb);
+  R = (min(R, kMaxScanRows) / 8) * 8;
+  if (R < 8) return cudaErrorNotSupported;
+  const uint32_t sb = std::max<uint32_t>(pps * pb, R * rb);
+  const int stages = max(32 / R, max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb))));
+  if (stages > kMaxStages) return cudaErrorNotSupported;
+  size_t ring = static_cast<size_t>(stages) * sb;
+  ring = max(ring, sizeof(TopkShared));
+  ring = max(ring, sizeof(float) * kConsumerWarps * G * (D + 2));
+  ring = (ring + 127) & ~static_cast<size_t>(127);
+  const size_t meta = sizeof(uint64_t) * 2 * kMaxStages +
+                      sizeof(int) * (kMaxStages + kMaxStages * kMaxPagesPerStage) +
+                      (sizeof(int) + sizeof(float)) * kMaxStages * kMaxScanRows;
+  const size_t keys_off = (ring + meta + 127) & ~static_cast<size_t>(127);
+  const size_t keys_bytes =
+      max(sizeof(uint32_t) * p.max_pages_per_seq, sizeof(float) * kMaxCluster * G * (D + 2));
+  const size_t sel_off = (keys_off + keys_bytes + 127) & ~static_cast<size_t>(127);
+  const size_t smem = sel_off + sizeof(int) * n_sel_pages(p);
+  a.stages = stages;
+  a.rows_per_stage = R;
+  a.pages_per_stage = pps;
+  a.stage_bytes = sb;
+  a.row_bytes = rb;
+  a.page_bytes = pb;
+  a.ring_bytes = static_cast<uint32_t>(ring);
+  a.keys_off = static_cast<uint32_t>(keys_off);
+  a.sel_off = static_cast<uint32_t>(sel_off);
+
+  auto kern = k_fused<T, TQ, D, G, 1>;  // int8 pools are only scored by the sketch selector
+  if constexpr (!is_i8<T>())
+    if (p.selector == SPG_SEL_QUEST) kern = k_fused<T, TQ, D, G, 0>;
+  cudaError_t e = ensure_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  // cluster size: 8 CTAs per unit when the GPU can hold them all at once,
+  // else 4 or 2, so that the grid stays within about one wave
+  const int units = p.batch * p.num_kv_heads;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int slots = device_sm_count() * per_sm;
+  int C = kMaxCluster;
+  while (C > 2 && units * C > slots) C /= 2;
+  a.cluster = C;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(C, units);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <typename T, typename TQ>
+cudaError_t fused_dispatch(const spg_params& p, const FusedArgs& a, cudaStream_t st) {
+  const int G = p.num_q_heads / p.num_kv_heads;
+#define SPG_FU(D_, G_) \
+  if (p.head_dim == D_ && G == G_) return fused_typed<T, TQ, D_, G_>(p, a, st);
+  SPG_FU(128, 1) SPG_FU(128, 2) SPG_FU(128, 4) SPG_FU(128, 8)
+  SPG_FU(64, 1) SPG_FU(64, 2) SPG_FU(64, 4) SPG_FU(64, 8)
+#undef SPG_FU
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+bool fused_supported(const spg_params& p, int append) {
+  if (p.selector != SPG_SEL_QUEST && p.selector != SPG_SEL_SKETCH_INT4) return false;
+  if (p.max_pages_per_seq > kFusedMaxPages) return false;
+  if (p.selector == SPG_SEL_SKETCH_INT4 && p.page_size > 128) return false;
+  if (append && (p.selector != SPG_SEL_QUEST || p.n_recent_pages < 1)) return false;
+  return true;
+}
+
+cudaError_t launch_fused(const spg_params& p, const void* q, const void* k_pool,
+                         const void* v_pool, const void* k_scale, const void* v_scale,
+                         const int32_t* page_table, const int32_t* seq_lens, void* minmax,
+                         const uint8_t* sketch, const float* sketch_scale, const float* proj,
+                         int32_t* sel, int32_t* sel_cnt, float* out, float* lse, int append,
+                         const Workspace& ws, cudaStream_t stream) {
+  FusedArgs a{};
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.k_scale = static_cast<const __half*>(k_scale);
+  a.v_scale = static_cast<const __half*>(v_scale);
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.minmax = minmax;
+  a.sketch = sketch;
+  a.sketch_scale = sketch_scale;
+  a.proj = proj;
+  a.sel = sel;
+  a.sel_cnt = sel_cnt;
+  a.out = out;
+  a.lse = lse;
+  a.err = ws.err;
+  a.Hkv = p.num_kv_heads;
+  a.S = p.page_size;
+  a.MP = p.max_pages_per_seq;
+  a.n_phys = p.num_phys_pages;
+  a.n_sink = p.n_sink_pages;
+  a.n_recent = p.n_recent_pages;
+  a.n_sel = n_sel_pages(p);
+  a.append = append;
+  const float scale = p.softmax_scale > 0.f ? p.softmax_scale
+                                            : 1.0f / sqrtf(static_cast<float>(p.head_dim));
+  a.scale_log2 = scale * kLog2e;
+  a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(p.head_dim));
+  switch (p.kv_dtype) {
+    case SPG_F16:
+      return fused_dispatch<__half, __half>(p, a, stream);
+    case SPG_BF16:
+      return fused_dispatch<__nv_bfloat16, __nv_bfloat16>(p, a, stream);
+    default:
+      if (p.q_dtype == SPG_F16) return fused_dispatch<int8_t, __half>(p, a, stream);
+      return fused_dispatch<int8_t, __nv_bfloat16>(p, a, stream);
+  }
+}
+
+}  // namespace spg

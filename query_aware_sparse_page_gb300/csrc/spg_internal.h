@@ -13,6 +13,7 @@ namespace spg {
 struct Workspace {
   int32_t* err;     // error word (header)
   int32_t* counters;  // [B][Hkv] split arrivals of the attention kernel; zero between calls
+  int32_t* sel_counters;  // [B][Hkv] scoring CTAs done, for the fused selection; zero between calls
   float* scores;    // [B][Hkv][MP]
   float* pm;        // [B][Hq][kMaxSplits] running max (log2 domain)
   float* pl;        // [B][Hq][kMaxSplits] running sum
@@ -31,13 +32,14 @@ cudaError_t launch_meta_update(const spg_params& p, const void* k_pool, const vo
                                void* minmax, uint8_t* sketch, float* sketch_scale,
                                const float* proj, int32_t* err, cudaStream_t stream);
 
-cudaError_t launch_score(const spg_params& p, const void* q, const int32_t* page_table,
-                         const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
-                         const float* sketch_scale, const float* proj, float* scores,
-                         int32_t* err, cudaStream_t stream);
-
-cudaError_t launch_topk(const spg_params& p, const float* scores, const int32_t* seq_lens,
-                        int32_t* sel, int32_t* sel_cnt, int32_t* err, cudaStream_t stream);
+// Scores every candidate page into `scores`; with sel != nullptr also
+// selects each unit's pages (inside the scoring launch, or in a separate
+// selection kernel for very long page tables).
+cudaError_t launch_select(const spg_params& p, const void* q, const int32_t* page_table,
+                          const int32_t* seq_lens, const void* minmax, const uint8_t* sketch,
+                          const float* sketch_scale, const float* proj, float* scores,
+                          int32_t* sel, int32_t* sel_cnt, const Workspace& ws,
+                          cudaStream_t stream);
 
 // sel == nullptr -> dense (every page of every sequence)
 cudaError_t launch_attention(const spg_params& p, const void* q, const void* k_pool,
@@ -45,5 +47,17 @@ cudaError_t launch_attention(const spg_params& p, const void* q, const void* k_p
                              const int32_t* page_table, const int32_t* seq_lens,
                              const int32_t* sel, const int32_t* sel_cnt, float* out, float* lse,
                              const Workspace& ws, cudaStream_t stream);
+
+// The whole step in one cluster launch (see spg_fused.cu).  fused_supported
+// says whether these parameters can take that path; launch_fused returns
+// cudaErrorNotSupported, before launching, when the page layout does not fit
+// its shared-memory plan.
+bool fused_supported(const spg_params& p, int append);
+cudaError_t launch_fused(const spg_params& p, const void* q, const void* k_pool,
+                         const void* v_pool, const void* k_scale, const void* v_scale,
+                         const int32_t* page_table, const int32_t* seq_lens, void* minmax,
+                         const uint8_t* sketch, const float* sketch_scale, const float* proj,
+                         int32_t* sel, int32_t* sel_cnt, float* out, float* lse, int append,
+                         const Workspace& ws, cudaStream_t stream);
 
 }  // namespace spg

@@ -17,12 +17,21 @@
 namespace spg {
 namespace {
 
-// Append, Quest: one warp per (batch, kv-head).
-template <typename T>
+// CPL consecutive elements moved as one 4- or 8-byte word
+template <typename T, int CPL>
+struct alignas(CPL * sizeof(T)) Vec {
+  T v[CPL];
+};
+
+// Append, Quest: one warp per (batch, kv-head); each lane owns CPL
+// consecutive channels of the new key and of the page's m and M rows.
+template <typename T, int CPL>
 __global__ void k_minmax_append(const T* __restrict__ k_pool, const int32_t* __restrict__ page_table,
                                 const int32_t* __restrict__ seq_lens, T* __restrict__ minmax,
                                 int B, int Hkv, int S, int d, int MP, int n_phys,
                                 int32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_trigger();
   const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= B * Hkv) return;
@@ -42,19 +51,25 @@ __global__ void k_minmax_append(const T* __restrict__ k_pool, const int32_t* __r
     if (lane == 0) record_error(err, SPG_DEVERR_PAGE_ID);
     return;
   }
-  const T* krow = k_pool + (((size_t)phys * Hkv + h) * S + slot) * d;
-  T* mrow = minmax + ((size_t)phys * Hkv + h) * 2 * d;
-  for (int c = lane; c < d; c += 32) {
-    const T k = krow[c];
-    if (slot == 0) {
-      mrow[c] = k;
-      mrow[d + c] = k;
-    } else {
-      const float kf = to_f32(k);
-      if (kf < to_f32(mrow[c])) mrow[c] = k;
-      if (kf > to_f32(mrow[d + c])) mrow[d + c] = k;
-    }
+  using V = Vec<T, CPL>;
+  const V k = *reinterpret_cast<const V*>(k_pool + (((size_t)phys * Hkv + h) * S + slot) * d +
+                                          lane * CPL);
+  V* lo = reinterpret_cast<V*>(minmax + ((size_t)phys * Hkv + h) * 2 * d + lane * CPL);
+  V* hi = reinterpret_cast<V*>(minmax + ((size_t)phys * Hkv + h) * 2 * d + d + lane * CPL);
+  if (slot == 0) {  // the page's first token starts its statistics
+    *lo = k;
+    *hi = k;
+    return;
   }
+  V m = *lo, M = *hi;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const float kf = to_f32(k.v[c]);
+    if (kf < to_f32(m.v[c])) m.v[c] = k.v[c];
+    if (kf > to_f32(M.v[c])) M.v[c] = k.v[c];
+  }
+  *lo = m;
+  *hi = M;
 }
 
 // Rebuild, Quest: one warp per (batch, kv-head, page).
@@ -196,10 +211,14 @@ cudaError_t meta_typed(const spg_params& p, const void* k_pool, const void* k_sc
   const T* kp = static_cast<const T*>(k_pool);
   if (p.selector == SPG_SEL_QUEST) {
     if (!rebuild) {
-      const int threads = 256, units = B * Hkv;
+      const int threads = 128, units = B * Hkv;
       const int blocks = (units * 32 + threads - 1) / threads;
-      k_minmax_append<T><<<blocks, threads, 0, st>>>(kp, pt, lens, static_cast<T*>(minmax), B, Hkv,
-                                                     S, d, MP, NP, err);
+      T* mm = static_cast<T*>(minmax);
+      if (d == 128)
+        return launch_pdl(k_minmax_append<T, 4>, dim3(blocks), dim3(threads), 0, st, kp, pt, lens,
+                          mm, B, Hkv, S, d, MP, NP, err);
+      return launch_pdl(k_minmax_append<T, 2>, dim3(blocks), dim3(threads), 0, st, kp, pt, lens,
+                        mm, B, Hkv, S, d, MP, NP, err);
     } else {
       const int wpb = 8;
       dim3 grid((MP + wpb - 1) / wpb, B * Hkv);
