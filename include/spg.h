@@ -45,13 +45,18 @@
  *   page_table   [B][MP] int32         physical page of each logical page
  *   seq_lens     [B] int32             tokens in each sequence, counting the
  *                                      token appended this step
- *   minmax       [P_phys][Hkv][2][d]   kv_dtype; [..][0][:] = per-channel
+ *   minmax       [B][Hkv][MP][2][d]    kv_dtype; per sequence, kv-head and
+ *                                      LOGICAL page: [..][0][:] = per-channel
  *                                      min m, [..][1][:] = max M of K over
  *                                      the page's valid tokens (Quest)
- *   sketch       [P_phys][Hkv][S][ds/2] uint8; int4 codes of the projected
- *                                      keys, two's complement, channel 2j in
- *                                      the low nibble of byte j (sketch)
- *   sketch_scale [P_phys][Hkv] fp32    one dequant scale per block (sketch)
+ *   sketch       [B][Hkv][MP][S][ds/2] uint8, per logical block; int4 codes
+ *                                      of the projected keys, two's
+ *                                      complement, channel 2j in the low
+ *                                      nibble of byte j (sketch)
+ *   sketch_scale [B][Hkv][MP] fp32     one dequant scale per block (sketch)
+ * Page metadata is kept in logical page order per sequence (not per physical
+ * page) so that scoring one (sequence, kv-head) reads a single contiguous
+ * range and needs no page-table lookup.
  *   proj         [d][ds] fp32          fixed projection P shared by all heads
  *   scores       [B][Hkv][MP] fp32     page scores; -inf for pages that are
  *                                      not candidates

@@ -16,9 +16,9 @@ _TORCH_KV = {0: torch.float16, 1: torch.bfloat16, 2: torch.int8}
 
 @dataclass
 class DecodeBuffers:
-    minmax: torch.Tensor | None  # [P_phys][Hkv][2][d]      (Quest)
-    sketch: torch.Tensor | None  # [P_phys][Hkv][S][ds/2]   (sketch)
-    sketch_scale: torch.Tensor | None  # [P_phys][Hkv]
+    minmax: torch.Tensor | None  # [B][Hkv][MP][2][d]      (Quest, logical pages)
+    sketch: torch.Tensor | None  # [B][Hkv][MP][S][ds/2]   (sketch, logical blocks)
+    sketch_scale: torch.Tensor | None  # [B][Hkv][MP]
     scores: torch.Tensor  # [B][Hkv][MP]
     sel: torch.Tensor  # [B][Hkv][n_sel]
     sel_cnt: torch.Tensor  # [B][Hkv]
@@ -34,10 +34,10 @@ def alloc_buffers(p, device="cuda") -> DecodeBuffers:
     n_sel = max(p.token_budget // S, 1)
     minmax = sketch = sketch_scale = None
     if p.selector == SEL_QUEST:
-        minmax = torch.zeros((NP, Hkv, 2, d), dtype=_TORCH_KV[p.kv_dtype], device=dev)
+        minmax = torch.zeros((B, Hkv, MP, 2, d), dtype=_TORCH_KV[p.kv_dtype], device=dev)
     elif p.selector == SEL_SKETCH_INT4:
-        sketch = torch.zeros((NP, Hkv, S, p.sketch_dim // 2), dtype=torch.uint8, device=dev)
-        sketch_scale = torch.zeros((NP, Hkv), dtype=torch.float32, device=dev)
+        sketch = torch.zeros((B, Hkv, MP, S, p.sketch_dim // 2), dtype=torch.uint8, device=dev)
+        sketch_scale = torch.zeros((B, Hkv, MP), dtype=torch.float32, device=dev)
     ws = torch.zeros(spg_workspace_size(p), dtype=torch.uint8, device=dev)
     return DecodeBuffers(
         minmax=minmax, sketch=sketch, sketch_scale=sketch_scale,

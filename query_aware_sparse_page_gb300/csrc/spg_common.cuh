@@ -244,24 +244,40 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Raises a kernel's dynamic shared-memory limit when it needs more than the
-// default 48 KB (once per kernel and size; repeated calls are no-ops).
+// Raises a kernel's dynamic shared-memory limit when its static plus dynamic
+// shared memory exceeds the default 48 KB (once per kernel and size;
+// repeated calls are no-ops).
 template <typename... KArgs>
 inline cudaError_t ensure_smem(void (*kern)(KArgs...), size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
   struct Entry {
     const void* fn;
     size_t bytes;
   };
-  static Entry cache[64];
+  static Entry cache[128];
   static int n = 0;
   const void* fn = reinterpret_cast<const void*>(kern);
   for (int i = 0; i < n; ++i)
     if (cache[i].fn == fn && cache[i].bytes >= bytes) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e == cudaSuccess && n < 64) cache[n++] = Entry{fn, bytes};
+  cudaFuncAttributes attr{};
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.sharedSizeBytes + bytes > 48 * 1024)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+  if (e == cudaSuccess && n < 128) cache[n++] = Entry{fn, bytes};
   return e;
+}
+
+// Quest metadata row layout: a row holds m (d channels) then M (d channels)
+// of one (sequence, kv-head, logical page); its 16-byte chunks are stored
+// XOR-swizzled by the page index, chunk j at j ^ (p % 8), so that 8
+// consecutive pages read at the same logical chunk hit 8 different bank
+// groups (conflict-free ldmatrix on a staged tile).  Element offset of
+// channel e (0 <= e < 2d) of page p's row:
+template <typename T>
+__host__ __device__ __forceinline__ int meta_swz(int e, int p) {
+  constexpr int EPC = 16 / static_cast<int>(sizeof(T));
+  return ((e / EPC) ^ (p & 7)) * EPC + (e % EPC);
 }
 
 // order-preserving map of an fp32 score to uint32 (larger float -> larger key)

@@ -10,11 +10,12 @@
 // indices never leave the chip here, they cross shared memory).
 //
 // Phases of one cluster (every CTA has 4 consumer warps and 1 producer warp):
-//  1. scan: the unit's candidate pages are split into 8 contiguous chunks.
-//     The producer resolves page ids (one lane per page) and streams the
-//     metadata rows of its chunk (Quest: m and M, 2*d elements; sketch: the
-//     block's int4 codes) into the shared-memory ring with cp.async.bulk,
-//     several rows per stage; the consumers score each row and store its
+//  1. scan: the unit's candidate pages are split into contiguous chunks, one
+//     per CTA.  Metadata is stored per sequence in logical page order, so a
+//     chunk's rows (Quest: m and M, 2*d elements; sketch: the block's int4
+//     codes) are one contiguous range; the producer streams it into the
+//     shared-memory ring with one cp.async.bulk per stage of up to 64 rows,
+//     and the consumers score each row and store its
 //     order-preserving key straight into the leader CTA's shared memory
 //     (distributed shared memory, st.shared::cluster).
 //  2. cluster barrier; the leader (rank 0) runs the exact top-k over the
@@ -99,18 +100,19 @@ __device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int 
   }
   const size_t ph = static_cast<size_t>(phys) * a.Hkv + h;
   const T* k = static_cast<const T*>(a.k_pool) + (ph * S + slot) * D + lane * CPL;
-  T* lo = static_cast<T*>(a.minmax) + ph * 2 * D + lane * CPL;
-  T* hi = lo + D;
+  T* row = static_cast<T*>(a.minmax) + ((static_cast<size_t>(b) * a.Hkv + h) * a.MP + p) * 2 * D;
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const T kv = k[c];
+    T& lo = row[meta_swz<T>(lane * CPL + c, p)];
+    T& hi = row[meta_swz<T>(D + lane * CPL + c, p)];
     if (slot == 0) {
-      lo[c] = kv;
-      hi[c] = kv;
+      lo = kv;
+      hi = kv;
     } else {
       const float kf = to_f32(kv);
-      if (kf < to_f32(lo[c])) lo[c] = kv;
-      if (kf > to_f32(hi[c])) hi[c] = kv;
+      if (kf < to_f32(lo)) lo = kv;
+      if (kf > to_f32(hi)) hi = kv;
     }
   }
 }
@@ -119,7 +121,6 @@ template <typename T, typename TQ, int D, int G, int SEL>
 __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const FusedArgs a) {
   constexpr int CW = kConsumerWarps;
   const int C = a.cluster;
-  constexpr int QCPL = D / 16;  // Quest scan: channels per lane of a half-warp
   using Consumer = AttnConsumer<T, D, G>;
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -136,8 +137,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
   uint64_t* empty = full + kMaxStages;
   int* s_np = reinterpret_cast<int*>(empty + kMaxStages);                // [stages] pages in stage
   int* s_nv = s_np + kMaxStages;                                          // [stages][8] valid tokens
-  int* s_rows = s_nv + kMaxStages * kMaxPagesPerStage;                    // [stages][64] scan rows
-  float* s_rsc = reinterpret_cast<float*>(s_rows + kMaxStages * kMaxScanRows);  // [stages][64]
+  float* s_rsc = reinterpret_cast<float*>(s_nv + kMaxStages * kMaxPagesPerStage);  // [stages][64]
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + a.keys_off);       // leader: keys
   float* s_part = reinterpret_cast<float*>(smem + a.keys_off);            // leader: partials
   int* s_sel = reinterpret_cast<int*>(smem + a.sel_off);                  // leader: selection
@@ -178,63 +178,36 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
   bool ok = true;
 
   if (warp == CW) {
-    // producer: one lane per row, so a batch of 32 rows is issued at once;
-    // the next batch's page ids are in flight while this one is issued
-    auto resolve = [&](int base, int& ph, float& sc) {
-      const int j = base + lane;
-      ph = -1;
-      sc = 0.f;
-      if (j < rows) {
-        ph = a.page_table[static_cast<size_t>(b) * a.MP + c0 + j];
-        if (ph < 0 || ph >= a.n_phys) {
-          record_error(a.err, SPG_DEVERR_PAGE_ID);
-          ph = -1;
-        } else if constexpr (SEL == 1) {
-          sc = __ldg(a.sketch_scale + static_cast<size_t>(ph) * Hkv + h);
-        }
-      }
-    };
-    int ph_cur, ph_nxt = -1;
-    float sc_cur, sc_nxt = 0.f;
-    resolve(0, ph_cur, sc_cur);
-    for (int base = 0; base < rows; base += 32) {
-      if (base + 32 < rows) resolve(base + 32, ph_nxt, sc_nxt);
-      const int i = base + lane, r = i % R, k = i / R, stage = k % STAGES;
-      const bool mine = i < rows;
-      // the lane holding a stage's first row waits until the slot is free
-      // (a batch spans at most STAGES stages, so every wait is one phase ahead)
+    // producer: metadata is stored in logical page order, so this CTA's rows
+    // are one contiguous range: one bulk copy per stage of R rows
+    const size_t lrow0 = static_cast<size_t>(unit) * a.MP + c0;
+    const uint8_t* src0 = SEL == 0 ? static_cast<const uint8_t*>(a.minmax) + lrow0 * rb
+                                   : a.sketch + lrow0 * rb;
+    for (int k = 0; k < n_scan; ++k) {
+      const int stage = k % STAGES, nr = min(R, rows - k * R);
       bool lok = true;
-      if (mine && r == 0 && k >= STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
-      if (!lok) record_error(a.err, SPG_DEVERR_TIMEOUT);
-      ok = __all_sync(0xffffffffu, lok) != 0;
-      if (!ok) break;
-      if (mine) {
-        s_rows[stage * kMaxScanRows + r] = ph_cur >= 0 ? c0 + i : -(c0 + i) - 1;
-        s_rsc[stage * kMaxScanRows + r] = sc_cur;
-        if (ph_cur >= 0) {
-          const uint8_t* src;
-          if constexpr (SEL == 0)
-            src = static_cast<const uint8_t*>(a.minmax) +
-                  (static_cast<size_t>(ph_cur) * Hkv + h) * 2 * D * sizeof(T);
-          else
-            src = a.sketch + (static_cast<size_t>(ph_cur) * Hkv + h) * S * 8;
-          mbar_expect_tx(&full[stage], rb);
-          bulk_g2s(ring + static_cast<size_t>(stage) * sbytes + r * rb, src, rb, &full[stage]);
-        }
+      if (lane == 0 && k >= STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
+        break;
       }
+      if (lane == 0) {
+        mbar_expect_tx(&full[stage], nr * rb);
+        bulk_g2s(ring + static_cast<size_t>(stage) * sbytes, src0 + static_cast<size_t>(k) * R * rb,
+                 nr * rb, &full[stage]);
+      }
+      if constexpr (SEL == 1)
+        for (int r = lane; r < nr; r += 32)
+          s_rsc[stage * kMaxScanRows + r] = __ldg(a.sketch_scale + lrow0 + k * R + r);
       __syncwarp();
-      // the lane holding a stage's last row closes it (after every expect_tx)
-      if (mine && (r == R - 1 || i == rows - 1)) mbar_arrive(&full[stage]);
-      ph_cur = ph_nxt;
-      sc_cur = sc_nxt;
+      if (lane == 0) mbar_arrive(&full[stage]);
     }
   } else {
     // consumers
     if constexpr (SEL == 0) {
-      float qf[G][QCPL];
-      const int hl = lane & 15, hwid = warp * 2 + (lane >> 4);
-      quest_query<T, D, G>(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
-                           hl, qf);
+      QuestMma<T, D, G> qm;
+      qm.init(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D, lane);
       for (int ks = 0; ks < n_scan; ++ks) {
         const int stage = ks % STAGES;
         if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
@@ -243,21 +216,16 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
           break;
         }
         const int nr = min(R, rows - ks * R);
-        const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
-        for (int r = hwid; r < R; r += 2 * CW) {  // R is a multiple of 8: both halves iterate together
-          const int enc = r < nr ? s_rows[stage * kMaxScanRows + r] : -1;
-          uint32_t wm[QCPL / 2], wM[QCPL / 2];
-          if (r < nr && enc >= 0) {
-            smem_chunk<T, QCPL>(st + r * rb + hl * QCPL * sizeof(T), wm);
-            smem_chunk<T, QCPL>(st + r * rb + (D + hl * QCPL) * sizeof(T), wM);
-          } else {
-#pragma unroll
-            for (int c = 0; c < QCPL / 2; ++c) wm[c] = wM[c] = 0u;
-          }
-          const float score = quest_bound<T, D, G>(qf, wm, wM);
-          if (r < nr && hl == 0) {
-            const int p = enc >= 0 ? enc : -enc - 1;
-            st_cluster_u32(keys_leader + 4u * (p - lo), score_key(enc >= 0 ? score : -INFINITY));
+        const T* st = reinterpret_cast<const T*>(ring + static_cast<size_t>(stage) * sbytes);
+        for (int ti = warp; ti * 16 < nr; ti += CW) {  // one 16-page tile per warp
+          const int pt0 = c0 + ks * R + ti * 16;
+          float s0, s1;
+          qm.tile(st + ti * 16 * 2 * D, pt0, lane, s0, s1);
+          if ((lane & 3) == 0) {
+            const int g = lane >> 2;
+            if (ti * 16 + g < nr) st_cluster_u32(keys_leader + 4u * (pt0 + g - lo), score_key(s0));
+            if (ti * 16 + g + 8 < nr)
+              st_cluster_u32(keys_leader + 4u * (pt0 + g + 8 - lo), score_key(s1));
           }
         }
         __syncwarp();
@@ -307,22 +275,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
         const int nr = min(R, rows - ks * R);
         const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
         for (int r = warp; r < nr; r += CW) {  // one warp per block
-          const int enc = s_rows[stage * kMaxScanRows + r];
-          float score = -INFINITY;
-          if (enc >= 0) {
-            uint2 wk[4];
+          uint2 wk[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (lane + 32 * k < S)
-                wk[k] = *reinterpret_cast<const uint2*>(st + r * rb + (lane + 32 * k) * 8);
-            const float cz =
-                __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r]), a.inv_sqrt_d);
-            score = sketch_block_score(wk, S, qc, cz);
-          }
-          if (lane == 0) {
-            const int p = enc >= 0 ? enc : -enc - 1;
-            st_cluster_u32(keys_leader + 4u * (p - lo), score_key(score));
-          }
+          for (int k = 0; k < 4; ++k)
+            if (lane + 32 * k < S)
+              wk[k] = *reinterpret_cast<const uint2*>(st + r * rb + (lane + 32 * k) * 8);
+          const float cz =
+              __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r]), a.inv_sqrt_d);
+          const float score = sketch_block_score(wk, S, qc, cz);
+          if (lane == 0) st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r - lo), score_key(score));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
@@ -489,8 +450,8 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   while (pps * 2 <= kMaxPagesPerStage && (pps * 2) * pb <= static_cast<uint32_t>(kStageBytesTarget))
     pps *= 2;
   int R = static_cast<int>(std::max<uint32_t>(pps * pb, kStageBytesTarget) / rb);
-  R = (min(R, kMaxScanRows) / 8) * 8;
-  if (R < 8) return cudaErrorNotSupported;
+  R = (min(R, kMaxScanRows) / 16) * 16;  // whole 16-page tensor-core tiles
+  if (R < 16) return cudaErrorNotSupported;
   const uint32_t sb = std::max<uint32_t>(pps * pb, R * rb);
   const int stages = max(32 / R, max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb))));
   if (stages > kMaxStages) return cudaErrorNotSupported;
@@ -500,7 +461,7 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   ring = (ring + 127) & ~static_cast<size_t>(127);
   const size_t meta = sizeof(uint64_t) * 2 * kMaxStages +
                       sizeof(int) * (kMaxStages + kMaxStages * kMaxPagesPerStage) +
-                      (sizeof(int) + sizeof(float)) * kMaxStages * kMaxScanRows;
+                      sizeof(float) * kMaxStages * kMaxScanRows;
   const size_t keys_off = (ring + meta + 127) & ~static_cast<size_t>(127);
   const size_t keys_bytes =
       max(sizeof(uint32_t) * p.max_pages_per_seq, sizeof(float) * kMaxCluster * G * (D + 2));

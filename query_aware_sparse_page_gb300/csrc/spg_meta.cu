@@ -5,6 +5,11 @@
 // a token is inserted.  The page's first token starts the statistics afresh,
 // so pages can be recycled without clearing.
 //
+// Metadata is stored per sequence in logical page order ([B][Hkv][MP][...]),
+// not per physical page: the scan of one (sequence, kv-head) then reads one
+// contiguous range, in large bulk copies, and needs no page-table lookup.
+// Quest rows are chunk-swizzled by page (meta_swz).
+//
 // Sketch (SALS长序列推理优化, 算法简介 "low rank 预处理" and QSI's int4 index
 // key): when a block of S tokens is complete, its keys are dequantised,
 // projected through the fixed d x ds matrix P (fp32, one rounded product and
@@ -54,8 +59,9 @@ __global__ void k_minmax_append(const T* __restrict__ k_pool, const int32_t* __r
   using V = Vec<T, CPL>;
   const V k = *reinterpret_cast<const V*>(k_pool + (((size_t)phys * Hkv + h) * S + slot) * d +
                                           lane * CPL);
-  V* lo = reinterpret_cast<V*>(minmax + ((size_t)phys * Hkv + h) * 2 * d + lane * CPL);
-  V* hi = reinterpret_cast<V*>(minmax + ((size_t)phys * Hkv + h) * 2 * d + d + lane * CPL);
+  const size_t mrow = ((size_t)unit * MP + p) * 2 * d;  // [B][Hkv][MP][2][d]
+  V* lo = reinterpret_cast<V*>(minmax + mrow + meta_swz<T>(lane * CPL, p));
+  V* hi = reinterpret_cast<V*>(minmax + mrow + meta_swz<T>(d + lane * CPL, p));
   if (slot == 0) {  // the page's first token starts its statistics
     *lo = k;
     *hi = k;
@@ -97,7 +103,7 @@ __global__ void k_minmax_rebuild(const T* __restrict__ k_pool, const int32_t* __
   }
   const int n_valid = min(S, L - p * S);
   const T* base = k_pool + ((size_t)phys * Hkv + h) * S * d;
-  T* mrow = minmax + ((size_t)phys * Hkv + h) * 2 * d;
+  T* mrow = minmax + ((size_t)unit * MP + p) * 2 * d;  // [B][Hkv][MP][2][d]
   for (int c = lane; c < d; c += 32) {
     T lo = base[c], hi = base[c];
     float lof = to_f32(lo), hif = lof;
@@ -107,8 +113,8 @@ __global__ void k_minmax_rebuild(const T* __restrict__ k_pool, const int32_t* __
       if (kf < lof) { lo = k; lof = kf; }
       if (kf > hif) { hi = k; hif = kf; }
     }
-    mrow[c] = lo;
-    mrow[d + c] = hi;
+    mrow[meta_swz<T>(c, p)] = lo;
+    mrow[meta_swz<T>(d + c, p)] = hi;
   }
 }
 
@@ -189,7 +195,8 @@ __global__ void k_sketch_block(const T* __restrict__ k_pool, const __half* __res
   const float scale = a > 0.f ? __fdiv_rn(a, 7.0f) : 1.0f;
 
   // codes, two per byte (channel 2j in the low nibble)
-  uint8_t* out = sketch + ph * S * (ds / 2);
+  const size_t lrow = (size_t)unit * MP + blk;  // [B][Hkv][MP] logical block
+  uint8_t* out = sketch + lrow * S * (ds / 2);
   for (int o2 = threadIdx.x; o2 < S * ds / 2; o2 += blockDim.x) {
     const float v0 = sV[2 * o2], v1 = sV[2 * o2 + 1];
     int c0 = static_cast<int>(rintf(__fdiv_rn(v0, scale)));
@@ -198,7 +205,7 @@ __global__ void k_sketch_block(const T* __restrict__ k_pool, const __half* __res
     c1 = max(-7, min(7, c1));
     out[o2] = static_cast<uint8_t>((c0 & 0xf) | ((c1 & 0xf) << 4));
   }
-  if (threadIdx.x == 0) sketch_scale[ph] = scale;
+  if (threadIdx.x == 0) sketch_scale[lrow] = scale;
 }
 
 template <typename T>

@@ -2,11 +2,10 @@
 //
 // Scoring streams one metadata row per candidate page:
 //  * Quest (Quest 完全拆解, 核心机制): score = max over the kv-head group's
-//    query heads of sum_i max(q_i m_i, q_i M_i).  Since M_i >= m_i the max is
-//    q_i * (q_i >= 0 ? M_i : m_i); the fp16/bf16 product is exact in fp32,
-//    only the channel sum rounds.  A half-warp covers one 2*d-element row
-//    with 16-byte loads; each half-warp scores 16 pages with the next batch
-//    of 4 rows already in flight while the current one is reduced.
+//    query heads of sum_i max(q_i m_i, q_i M_i) = sum_i q-_i m_i + q+_i M_i
+//    (q- = min(q, 0), q+ = max(q, 0)): a [pages x 2d] x [2d x G] product,
+//    scored 16 pages at a time on the tensor cores (QuestMma) from rows
+//    staged in shared memory by one bulk copy per CTA.
 //  * Sketch (SALS长序列推理优化, QSI steps 1-3): the group-mean query is
 //    projected through P and quantised to int8 (same fp32 rule as the keys),
 //    the int4 key codes are unpacked to int8 lanes and dotted with dp4a
@@ -32,7 +31,7 @@
 namespace spg {
 namespace {
 
-constexpr int kQuestPagesPerCta = 256;  // 16 half-warps x 16 pages
+constexpr int kQuestPagesPerCta = 64;  // 4 warps x one 16-page tile
 constexpr int kSketchBlocksPerCta = 8;  // one warp per block
 constexpr int kFusedTopkMaxPages = 8192;
 
@@ -101,72 +100,57 @@ __device__ __forceinline__ int seq_pages(const SelectArgs& a, int b, int* L_out)
   return (L + a.S - 1) / a.S;
 }
 
-// Quest scores (+ fused selection): grid (ceil(MP/256), B*Hkv), 256 threads.
+// Quest scores (+ fused selection): grid (ceil(MP/64), B*Hkv), 128 threads.
+// The CTA's 64 metadata rows are one contiguous range (logical page order):
+// one bulk copy stages them, then each warp scores one 16-page tile on the
+// tensor cores while the next CTAs' copies are in flight.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(256) k_quest_select(const SelectArgs a, int fused) {
-  constexpr int CPL = D / 16;  // channels per lane; 16 lanes cover one row
-  constexpr int PPH = 16;      // pages per half-warp
-  constexpr int BT = 4;        // pages per batch (one batch in flight ahead)
-  extern __shared__ uint32_t s_keys[];
-  __shared__ int s_phys[kQuestPagesPerCta];
+__global__ void __launch_bounds__(128) k_quest_select(const SelectArgs a, int fused) {
+  constexpr int RB = 2 * D * static_cast<int>(sizeof(T));  // bytes of one metadata row
+  extern __shared__ __align__(128) uint8_t smem[];
+  T* rows = reinterpret_cast<T*>(smem);                                    // [64][2d]
+  uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + kQuestPagesPerCta * RB);  // fused top-k
+  __shared__ __align__(8) uint64_t bar;
   __shared__ TopkShared s_t;
   __shared__ int s_last;
 
   pdl_wait();
   const int unit = blockIdx.y, Hkv = a.Hkv;
   const int b = unit / Hkv, h = unit % Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p0 = blockIdx.x * kQuestPagesPerCta;
   int L;
   const int P = seq_pages(a, b, &L);
   const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo);
-
-  for (int i = threadIdx.x; i < kQuestPagesPerCta; i += blockDim.x) {
-    const int p = p0 + i;
-    int ph = -1;
-    if (p >= lo && p < hi) {
-      ph = a.page_table[static_cast<size_t>(b) * a.MP + p];
-      if (ph < 0 || ph >= a.n_phys) {
-        record_error(a.err, SPG_DEVERR_PAGE_ID);
-        ph = -1;
-      }
-    }
-    s_phys[i] = ph;
+  const int n_rows = max(0, min(kQuestPagesPerCta, P - p0));
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
   }
-  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
-  float qf[G][CPL];
-  quest_query<T, D, G>(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hkv * G + h * G) * D,
-                       hl, qf);
   __syncthreads();
-
-  const T* mm = static_cast<const T*>(a.minmax);
-  uint32_t wm[2][BT][CPL / 2], wM[2][BT][CPL / 2];
-  int phs[2][BT];
-  auto load_batch = [&](int bt, int buf) {
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(n_rows) * RB);
+    if (n_rows > 0)
+      bulk_g2s(rows,
+               static_cast<const T*>(a.minmax) + (static_cast<size_t>(unit) * a.MP + p0) * 2 * D,
+               static_cast<uint32_t>(n_rows) * RB, &bar);
+  }
+  QuestMma<T, D, G> qm;
+  qm.init(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hkv * G + h * G) * D, lane);
+  if (!mbar_wait_bounded(&bar, 0)) {
+    if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
+    mbar_wait_bounded(&bar, 0);  // drain before the CTA may leave
+  }
+  float s0, s1;
+  qm.tile(rows + warp * 16 * 2 * D, p0 + warp * 16, lane, s0, s1);
+  if ((lane & 3) == 0) {
+    const int g = lane >> 2;
 #pragma unroll
-    for (int i = 0; i < BT; ++i) {
-      const int ph = s_phys[hw * PPH + bt * BT + i];
-      phs[buf][i] = ph;
-      if (ph >= 0) {
-        const T* row = mm + (static_cast<size_t>(ph) * Hkv + h) * 2 * D + hl * CPL;
-        load_row_chunk<T, CPL>(row, wm[buf][i]);
-        load_row_chunk<T, CPL>(row + D, wM[buf][i]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < CPL / 2; ++c) wm[buf][i][c] = wM[buf][i][c] = 0u;
-      }
-    }
-  };
-  load_batch(0, 0);
-#pragma unroll
-  for (int bt = 0; bt < PPH / BT; ++bt) {
-    const int buf = bt & 1;
-    if (bt + 1 < PPH / BT) load_batch(bt + 1, buf ^ 1);
-#pragma unroll
-    for (int i = 0; i < BT; ++i) {
-      const float best = quest_bound<T, D, G>(qf, wm[buf][i], wM[buf][i]);
-      const int p = p0 + hw * PPH + bt * BT + i;
-      if (hl == 0 && p < a.MP)
-        a.scores[static_cast<size_t>(unit) * a.MP + p] = phs[buf][i] >= 0 ? best : -INFINITY;
+    for (int half = 0; half < 2; ++half) {
+      const int p = p0 + warp * 16 + g + 8 * half;
+      if (p < a.MP)
+        a.scores[static_cast<size_t>(unit) * a.MP + p] =
+            (p >= lo && p < hi) ? (half ? s1 : s0) : -INFINITY;
     }
   }
   pdl_trigger();
@@ -194,20 +178,14 @@ __global__ void __launch_bounds__(256) k_sketch_select(const SelectArgs a, int f
   int L;
   const int P = seq_pages(a, b, &L);
   const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo);
-  int ph = -1;
-  if (blk >= lo && blk < hi) {
-    ph = a.page_table[static_cast<size_t>(b) * a.MP + blk];
-    if (ph < 0 || ph >= a.n_phys) {
-      if (lane == 0) record_error(a.err, SPG_DEVERR_PAGE_ID);
-      ph = -1;
-    }
-  }
+  const int ph = (blk >= lo && blk < hi) ? blk : -1;  // candidate (logical block)
   // this warp's block codes and scale, in flight while the index query is built
-  const size_t row0 = (static_cast<size_t>(ph < 0 ? 0 : ph) * Hkv + h) * S;
+  const size_t lrow = static_cast<size_t>(unit) * a.MP + (ph < 0 ? 0 : ph);
+  const size_t row0 = lrow * S;
   uint2 wk[4];
   float sk = 1.f;
   if (ph >= 0) {
-    sk = __ldg(a.sketch_scale + static_cast<size_t>(ph) * Hkv + h);
+    sk = __ldg(a.sketch_scale + lrow);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int t = lane + 32 * k;
@@ -245,17 +223,18 @@ __global__ void __launch_bounds__(1024) k_topk(const SelectArgs a) {
 }
 
 template <typename T>
-cudaError_t quest_typed(const spg_params& p, const SelectArgs& a, int fused, size_t smem,
+cudaError_t quest_typed(const spg_params& p, const SelectArgs& a, int fused, size_t smem_keys,
                         cudaStream_t st) {
   dim3 grid((p.max_pages_per_seq + kQuestPagesPerCta - 1) / kQuestPagesPerCta,
             p.batch * p.num_kv_heads);
   const int G = a.G;
+  const size_t smem = static_cast<size_t>(kQuestPagesPerCta) * 2 * p.head_dim * sizeof(T) + smem_keys;
 #define SPG_QS(D_, G_)                                                                     \
   if (p.head_dim == D_ && G == G_) {                                                        \
     auto kern = k_quest_select<T, D_, G_>;                                                  \
     cudaError_t e = ensure_smem(kern, smem);                                                \
     if (e != cudaSuccess) return e;                                                         \
-    return launch_pdl(kern, grid, dim3(256), smem, st, a, fused);                           \
+    return launch_pdl(kern, grid, dim3(128), smem, st, a, fused);                           \
   }
   SPG_QS(128, 1) SPG_QS(128, 2) SPG_QS(128, 4) SPG_QS(128, 8)
   SPG_QS(64, 1) SPG_QS(64, 2) SPG_QS(64, 4) SPG_QS(64, 8)

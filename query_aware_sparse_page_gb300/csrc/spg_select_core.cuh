@@ -210,6 +210,106 @@ __device__ __forceinline__ float quest_bound(const float (&qf)[G][D / 16], const
   return best;
 }
 
+// ---- Quest bound on tensor cores -------------------------------------------
+// With q- = min(q, 0) and q+ = max(q, 0), max(q m, q M) = q- m + q+ M exactly
+// (M >= m), so the bounds of a tile of 16 pages for the G query rows of a
+// group are one [16 x 2d] x [2d x G] product: A = the tile's metadata rows
+// (m then M, staged in shared memory), B = [q-; q+] (G columns, zero-padded
+// to 8).  mma.sync m16n8k16 with fp16/bf16 operands (q-/q+ are q or 0, so
+// exact) and fp32 accumulation; ldmatrix reads the chunk-swizzled rows
+// without bank conflicts.  The group score of a page is the max over its G
+// columns.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+template <typename T>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  if constexpr (std::is_same<T, __half>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+template <typename T, int D, int G>
+struct QuestMma {
+  static constexpr int KS = 2 * D / 16;  // k-steps over m then M
+  uint32_t bf[KS][2];                    // B fragments (q-; q+), one column per query row
+
+  // qrows: the group's G query rows (global); lane layout of the B fragment:
+  // column n = lane / 4, k pairs (2t, 2t+1) and (2t+8, 2t+9), t = lane % 4
+  __device__ void init(const T* qrows, int lane) {
+    const int n = lane >> 2, t = lane & 3;
+    const T zero = static_cast<T>(0.f);
+#pragma unroll
+    for (int j = 0; j < KS; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        T v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 16 * j + 2 * t + 8 * hf + e;
+          v[e] = zero;
+          if (n < G) {
+            const T qv = qrows[n * D + (k < D ? k : k - D)];
+            const float f = to_f32(qv);
+            v[e] = (k < D) ? (f < 0.f ? qv : zero) : (f > 0.f ? qv : zero);
+          }
+        }
+        bf[j][hf] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&v[0])) |
+                    (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&v[1])) << 16);
+      }
+  }
+
+  // 16 pages whose rows start at `rows` (shared memory, row stride 2d), the
+  // first being logical page p0.  Lanes with lane % 4 == 0 return the group
+  // score of tile row lane/4 in s0 and of row lane/4 + 8 in s1.
+  __device__ void tile(const T* rows, int p0, int lane, float& s0, float& s1) const {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int mi = lane >> 3, r = (mi & 1) * 8 + (lane & 7);
+    const int key = (p0 + r) & 7;
+    const uint32_t base = smem_u32(rows + r * 2 * D);
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      uint32_t a[4];
+      ldmatrix_x4(a, base + ((((2 * j) + (mi >> 1)) ^ key) << 4));
+      mma_16816<T>(c, a, bf[j][0], bf[j][1]);
+    }
+    const int t = lane & 3;
+    float m0 = -FLT_MAX, m1 = -FLT_MAX;
+    if (2 * t < G) {
+      m0 = c[0];
+      m1 = c[2];
+    }
+    if (2 * t + 1 < G) {
+      m0 = fmaxf(m0, c[1]);
+      m1 = fmaxf(m1, c[3]);
+    }
+    if constexpr (G > 2) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+    }
+    if constexpr (G > 4) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+    }
+    s0 = m0;
+    s1 = m1;
+  }
+};
+
 // the group's query rows for the lane's CPL channels (half-warp layout)
 template <typename T, int D, int G>
 __device__ __forceinline__ void quest_query(const T* qrows, int hl, float (&qf)[G][D / 16]) {

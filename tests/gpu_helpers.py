@@ -43,6 +43,18 @@ def run_step(inp, selector=None, n_sel_pages=None, fused=True, rebuild=True, buf
     return p, bufs, err
 
 
+def unswizzle_meta_row(row, p, elem_bytes=2):
+    """A Quest metadata row as stored (16-byte chunks XOR-swizzled by page p)
+    back in channel order: [2][d] (m, then M).  elem_bytes: size of one
+    stored element (2 for fp16/bf16, whatever dtype `row` was widened to)."""
+    row = np.asarray(row)
+    flat = row.reshape(-1)
+    epc = 16 // elem_bytes
+    chunks = flat.reshape(-1, epc)
+    perm = [c ^ (p & 7) for c in range(chunks.shape[0])]
+    return chunks[perm].reshape(row.shape)
+
+
 def gpu_selection(bufs, b, h):
     cnt = int(bufs.sel_cnt[b, h])
     row = bufs.sel[b, h].cpu().tolist()
