@@ -52,9 +52,9 @@ struct LaneChannels {
   }
 };
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, int NW = kConsumerWarps>
 struct AttnConsumer {
-  static constexpr int CW = kConsumerWarps;
+  static constexpr int CW = NW;  // warps sharing one staged page
   static constexpr int LPT = G >= 4 ? 16 : 8;  // lanes per token
   static constexpr int TPR = 32 / LPT;         // tokens per warp per round
   static constexpr int RT = CW * TPR;          // tokens per round of the whole stage
@@ -64,7 +64,9 @@ struct AttnConsumer {
   float qf[G][CPL], acc[G][CPL], m[G], l[G];
   int cw, tg, lt;
 
-  // qrows: the group's G query rows of D elements (global); scale folded in
+  // qrows: the group's G query rows of D elements (global); scale folded in.
+  // cw_: this warp's consumer index (its merge slot); its share of each page
+  // is cw_ % NW.
   template <typename TQ>
   __device__ void init(const TQ* qrows, float scale_log2, int cw_, int lane) {
     cw = cw_;
@@ -96,7 +98,7 @@ struct AttnConsumer {
       float z[4][G];
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
-        const int t = r0 + rr * RT + cw * TPR + tg;
+        const int t = r0 + rr * RT + (cw % NW) * TPR + tg;
 #pragma unroll
         for (int g = 0; g < G; ++g) z[rr][g] = -INFINITY;
         if (r0 + rr * RT < nv) {  // warp-uniform
@@ -132,7 +134,7 @@ struct AttnConsumer {
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         if (r0 + rr * RT < nv) {
-          const int t = r0 + rr * RT + cw * TPR + tg;
+          const int t = r0 + rr * RT + (cw % NW) * TPR + tg;
           const int tr = min(t, S - 1);
           float vf[CPL];
           LC::load(Vs + tr * D, lt, vf);
@@ -180,6 +182,184 @@ struct AttnConsumer {
 #pragma unroll
           for (int e = 0; e < LC::EPL; ++e)
             s_acc[(cw * G + g) * D + LC::base(lt, k) + e] = acc[g][k * LC::EPL + e];
+      }
+    }
+  }
+};
+
+// ---- tensor-core consumer ------------------------------------------------------
+// Flash-decoding of one staged page on the tensor cores (mma.sync m16n8k16,
+// fp32 accumulate) for fp16/bf16 pools, one warp per page.  The group's G
+// query rows are the N = 8 columns (zero-padded), tokens and channels the M
+// side, so the accumulators are small:
+//   S^T [16 tokens x 8 rows]    = K [16 x D] . Q^T [D x 8]       (A = K tile)
+//   O^T [D x 8 rows]           += V^T [D x 16 tokens] . P^T [16 x 8]
+// K and V come from ldmatrix (V transposed on load); P^T is rounded to the
+// pool's 16-bit type as a hi + lo pair (two products, ~16 significant bits
+// or more) and moved into the B layout with movmatrix.  The staged page is
+// D / 64 tiles of [S rows][64 channels] each for K, then the same for V, as
+// the TMA tile copy with 128-byte swizzle leaves them: the 16-byte chunk c of
+// row r sits at chunk c ^ (r % 8) of the row (tiles 1024-byte aligned).
+//
+// Lane layout (g = lane / 4, t = lane % 4): the lane owns query rows 2t and
+// 2t + 1: its running max m[e] and sum l[e], and accumulator columns e of
+// channels 16 mt + g and 16 mt + g + 8.
+template <typename T, int D, int G>
+struct AttnMma {
+  static_assert(D % 64 == 0, "64-channel tiles");
+  static constexpr int KS = D / 16;  // k-steps of Q K^T, m-tiles of P V
+  uint32_t qb[KS][2];
+  float acc[KS][4];
+  float m[2], l[2];
+  float scale;
+  int cw;
+
+  template <typename TQ>
+  __device__ void init(const TQ* qrows, float scale_log2, int cw_, int lane) {
+    static_assert(sizeof(TQ) == sizeof(T) && !is_i8<T>(), "same 16-bit type for q and K/V");
+    cw = cw_;
+    scale = scale_log2;
+    const int n = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < KS; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w = 0;
+        if (n < G) {
+          const int k = 16 * j + 2 * t + 8 * hf;
+          w = *reinterpret_cast<const uint32_t*>(qrows + n * D + k);
+        }
+        qb[j][hf] = w;
+      }
+#pragma unroll
+    for (int j = 0; j < KS; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // one staged page (shared memory, 1024-byte aligned) with nv valid tokens
+  // (0 < nv <= S, S a multiple of 16); the slots past nv are zeroed first
+  // when the page is the sequence's last, partial one
+  __device__ void consume(uint8_t* st, int S, int nv, int lane) {
+    constexpr int NH = D / 64;
+    const uint32_t kb = smem_u32(st);
+    const uint32_t vb = kb + static_cast<uint32_t>(S) * D * sizeof(T);
+    const uint32_t hs = static_cast<uint32_t>(S) * 128u;  // bytes of one 64-channel tile
+    if (nv < S) {
+      // rows past the end hold whatever the pool holds: make them zeros so
+      // that p = 0 times them stays 0 in the P V product
+      const int words = (S - nv) * NH * 8;
+      for (int i = lane; i < words; i += 32) {
+        const int r = nv + i / (NH * 8), rem = i % (NH * 8);
+        *reinterpret_cast<uint4*>(st + S * D * sizeof(T) + (rem >> 3) * hs + r * 128 + (rem & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    for (int t0 = 0; t0 < nv; t0 += 16) {
+      // S^T tile: two accumulation chains over the k-steps
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int tok = t0 + (mi & 1) * 8 + r8;  // A rows: tokens
+        const uint32_t rowb = kb + tok * 128u;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          const int chunk = 2 * j + (mi >> 1);
+          uint32_t a[4];
+          ldmatrix_x4(a, rowb + (chunk >> 3) * hs + (((chunk & 7) ^ (tok & 7)) << 4));
+          if (j & 1)
+            mma_16816<T>(c1, a, qb[j][0], qb[j][1]);
+          else
+            mma_16816<T>(c0, a, qb[j][0], qb[j][1]);
+        }
+      }
+      float sv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sv[e] = (c0[e] + c1[e]) * scale;
+      if (t0 + 16 > nv) {
+        if (t0 + g >= nv) sv[0] = sv[1] = -INFINITY;
+        if (t0 + g + 8 >= nv) sv[2] = sv[3] = -INFINITY;
+      }
+      // running max of rows 2t, 2t+1 over this tile's tokens (lanes with equal t)
+      float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      if (mx0 > m[0]) {
+        const float corr = exp2f(m[0] - mx0);
+        m[0] = mx0;
+        l[0] *= corr;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          acc[j][0] *= corr;
+          acc[j][2] *= corr;
+        }
+      }
+      if (mx1 > m[1]) {
+        const float corr = exp2f(m[1] - mx1);
+        m[1] = mx1;
+        l[1] *= corr;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          acc[j][1] *= corr;
+          acc[j][3] *= corr;
+        }
+      }
+      const float p0 = exp2f(sv[0] - m[0]), p1 = exp2f(sv[1] - m[1]);
+      const float p2 = exp2f(sv[2] - m[0]), p3 = exp2f(sv[3] - m[1]);
+      l[0] += p0 + p2;
+      l[1] += p1 + p3;
+      // P^T as B fragments: hi and lo 16-bit parts, tokens 0-7 and 8-15
+      const uint32_t h01 = pack2<T>(p0, p1), h23 = pack2<T>(p2, p3);
+      const float2 f01 = unpack2f<T>(h01), f23 = unpack2f<T>(h23);
+      const uint32_t l01 = pack2<T>(p0 - f01.x, p1 - f01.y), l23 = pack2<T>(p2 - f23.x, p3 - f23.y);
+      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+      const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+      {
+        const int tok = t0 + (mi >> 1) * 8 + r8;  // stored rows of the transposed loads
+        const uint32_t rowb = vb + tok * 128u;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          const int chunk = 2 * j + (mi & 1);
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, rowb + (chunk >> 3) * hs + (((chunk & 7) ^ (tok & 7)) << 4));
+          mma_16816<T>(acc[j], a, bh0, bh1);
+          mma_16816<T>(acc[j], a, bl0, bl1);
+        }
+      }
+    }
+  }
+
+  // the sums of rows 2t, 2t+1 over the warp's lanes (the max is already uniform)
+  __device__ void fold() {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+    }
+  }
+
+  // this warp's state into s_m/s_l [CW][G] and s_acc [CW][G][D]
+  __device__ void store(float* s_m, float* s_l, float* s_acc, int lane) const {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = 2 * t + e;
+      if (row < G) {
+        if (g == 0) {
+          s_m[cw * G + row] = m[e];
+          s_l[cw * G + row] = l[e];
+        }
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          s_acc[(cw * G + row) * D + 16 * j + g] = acc[j][e];
+          s_acc[(cw * G + row) * D + 16 * j + g + 8] = acc[j][e + 2];
+        }
       }
     }
   }

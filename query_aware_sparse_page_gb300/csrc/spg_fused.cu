@@ -49,6 +49,7 @@ constexpr int kStageBytesTarget = 16 * 1024;
 constexpr int kRingBytesTarget = 64 * 1024;
 
 struct FusedArgs {
+  CUtensorMap tmk, tmv;  // K / V pools as page tiles (fp16/bf16 pools)
   const void* q;
   const void* k_pool;
   const void* v_pool;
@@ -118,12 +119,16 @@ __device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int 
 }
 
 template <typename T, typename TQ, int D, int G, int SEL>
-__global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const FusedArgs a) {
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
+    k_fused(const __grid_constant__ FusedArgs a) {
   constexpr int CW = kConsumerWarps;
+  constexpr bool MMA = !is_i8<T>();  // tensor-core consumer, TMA tile producer
   const int C = a.cluster;
-  using Consumer = AttnConsumer<T, D, G>;
+  using Consumer = std::conditional_t<MMA, AttnMma<T, D, G>, AttnConsumer<T, D, G, 1>>;
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // TMA tiles with 128-byte swizzle want 1024-byte aligned destinations
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ float s_qbar[SEL ? 256 : 1];
   __shared__ float s_P[SEL ? 256 * 16 : 1];
   __shared__ int s_qc[4];
@@ -147,12 +152,21 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
   const int unit = blockIdx.y;
   const int Hkv = a.Hkv, b = unit / Hkv, h = unit % Hkv, Hq = Hkv * G;
 
+  // every stage has one owner: scan stage / attention stage k belongs to
+  // consumer warp k % CW (STAGES is a multiple of CW, so a ring slot always
+  // has the same owner)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CW);
+      mbar_init(&empty[s], 1);
     }
     mbar_fence_init();
+  }
+  if constexpr (MMA) {
+    if (threadIdx.x == CW * 32) {
+      tma_prefetch_desc(&a.tmk);
+      tma_prefetch_desc(&a.tmv);
+    }
   }
   pdl_wait();
   int L = a.seq_lens[b];
@@ -178,6 +192,13 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
   bool ok = true;
 
   if (warp == CW) {
+    if (rank == C - 1 && lane == 0 && P > 0) {
+      // the attend phase looks the selected pages up in this row: have it in
+      // L2 by then
+      const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.MP;
+      const uint32_t bytes = (static_cast<uint32_t>(P) * 4u) & ~15u;  // within the row
+      if ((reinterpret_cast<uintptr_t>(pt) & 15u) == 0 && bytes > 0) bulk_prefetch_l2(pt, bytes);
+    }
     // producer: metadata is stored in logical page order, so this CTA's rows
     // are one contiguous range: one bulk copy per stage of R rows
     const size_t lrow0 = static_cast<size_t>(unit) * a.MP + c0;
@@ -208,7 +229,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
     if constexpr (SEL == 0) {
       QuestMma<T, D, G> qm;
       qm.init(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D, lane);
-      for (int ks = 0; ks < n_scan; ++ks) {
+      for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
         if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
           if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
@@ -217,7 +238,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
         }
         const int nr = min(R, rows - ks * R);
         const T* st = reinterpret_cast<const T*>(ring + static_cast<size_t>(stage) * sbytes);
-        for (int ti = warp; ti * 16 < nr; ti += CW) {  // one 16-page tile per warp
+        for (int ti = 0; ti * 16 < nr; ++ti) {  // the stage's 16-page tiles
           const int pt0 = c0 + ks * R + ti * 16;
           float s0, s1;
           qm.tile(st + ti * 16 * 2 * D, pt0, lane, s0, s1);
@@ -265,7 +286,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
       consumers_sync();
       const int qc[4] = {s_qc[0], s_qc[1], s_qc[2], s_qc[3]};
       const float sq = s_sq;
-      for (int ks = 0; ks < n_scan; ++ks) {
+      for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
         if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
           if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
@@ -274,7 +295,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
         }
         const int nr = min(R, rows - ks * R);
         const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
-        for (int r = warp; r < nr; r += CW) {  // one warp per block
+        for (int r = 0; r < nr; ++r) {  // the stage's blocks
           uint2 wk[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -360,11 +381,21 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
           if (ph >= 0) {
             const size_t row = static_cast<size_t>(ph) * Hkv + h;
             mbar_expect_tx(&full[stage], 2 * tile + 2 * scb);
-            bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
-            bulk_g2s_hint(dst + tile, vpool + row * S * D, tile, &full[stage], pol);
-            if constexpr (is_i8<T>()) {
-              bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
-              bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
+            if constexpr (MMA) {
+              // D / 64 swizzled tiles of [S][64] for K, then for V
+              const int y = static_cast<int>(row) * S;
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf) {
+                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * 64, y, &full[stage], pol);
+                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * 64, y, &full[stage], pol);
+              }
+            } else {
+              bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
+              bulk_g2s_hint(dst + tile, vpool + row * S * D, tile, &full[stage], pol);
+              if constexpr (is_i8<T>()) {
+                bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
+                bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
+              }
             }
           }
         }
@@ -384,7 +415,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
     cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
               a.scale_log2, warp, lane);
     const int n_att_st = (n_att + PPS - 1) / PPS;
-    for (int ka = 0; ka < n_att_st && ok; ++ka) {
+    // this warp's attention stages: k = n_scan + ka with k % CW == warp
+    const int ka0 = ((warp - n_scan) % CW + CW) % CW;
+    for (int ka = ka0; ka < n_att_st && ok; ka += CW) {
       const int k = n_scan + ka, stage = k % STAGES;
       if (!mbar_wait_bounded(&full[stage], (k / STAGES) & 1)) {
         if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
@@ -393,10 +426,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_fused(const Fused
       const int np = s_np[stage];
       for (int i = 0; i < np; ++i) {
         const int nv = s_nv[stage * kMaxPagesPerStage + i];
-        if (nv > 0)
-          cons.consume(ring + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes, S,
-                       nv);
+        uint8_t* pg = ring + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes;
+        if (nv > 0) {
+          if constexpr (MMA)
+            cons.consume(pg, S, nv, lane);
+          else
+            cons.consume(pg, S, nv);
+        }
       }
+      if constexpr (MMA) fence_proxy_async();  // zeroed slots before the next TMA write
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
@@ -453,7 +491,9 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   R = (min(R, kMaxScanRows) / 16) * 16;  // whole 16-page tensor-core tiles
   if (R < 16) return cudaErrorNotSupported;
   const uint32_t sb = std::max<uint32_t>(pps * pb, R * rb);
-  const int stages = max(32 / R, max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb))));
+  // a multiple of the consumer warps: each ring slot has one owner
+  int stages = max(32 / R, max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb))));
+  stages = (stages + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
   if (stages > kMaxStages) return cudaErrorNotSupported;
   size_t ring = static_cast<size_t>(stages) * sb;
   ring = max(ring, sizeof(TopkShared));
@@ -466,7 +506,14 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   const size_t keys_bytes =
       max(sizeof(uint32_t) * p.max_pages_per_seq, sizeof(float) * kMaxCluster * G * (D + 2));
   const size_t sel_off = (keys_off + keys_bytes + 127) & ~static_cast<size_t>(127);
-  const size_t smem = sel_off + sizeof(int) * n_sel_pages(p);
+  const size_t smem = 1024 + sel_off + sizeof(int) * n_sel_pages(p);  // + alignment slack
+  if (smem > 227u * 1024u) return cudaErrorNotSupported;
+  if constexpr (!is_i8<T>()) {
+    const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
+    if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S) ||
+        !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S))
+      return cudaErrorNotSupported;
+  }
   a.stages = stages;
   a.rows_per_stage = R;
   a.pages_per_stage = pps;

@@ -1,6 +1,7 @@
 // Host-side launchers shared between the kernel files and the C ABI layer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -21,6 +22,14 @@ struct Workspace {
 };
 
 size_t workspace_bytes(const spg_params& p);
+
+// Tensor map of a K or V pool viewed as a 2-D array [rows][head_dim]
+// (rows = num_phys_pages * num_kv_heads * page_size) whose tile is one page
+// of one kv-head, 64 channels wide (128 bytes, 128-byte swizzle): a page is
+// copied as head_dim / 64 tiles.  False when the pool cannot be described
+// (dtype, alignment, size) or the encoder is unavailable.
+bool make_kv_tmap(CUtensorMap* map, const void* pool, int kv_dtype, long long rows, int head_dim,
+                  int page_size);
 Workspace carve_workspace(const spg_params& p, void* ws);
 
 int n_sel_pages(const spg_params& p);

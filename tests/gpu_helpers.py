@@ -14,6 +14,27 @@ from conftest import to_numpy
 TOL_OUT = {"f16": 2e-3, "bf16": 2e-3, "i8": 5e-3}  # max-abs on out and lse
 REL_GAP = 1e-5  # k-th / (k+1)-th oracle score gap under which several selections are correct
 
+# Two GPU paths over the same selection differ only by arithmetic order, and
+# by the tensor-core path rounding the probabilities P to the pool's 16-bit
+# type as a hi + lo pair: |p - hi - lo| <= 2^-(2 s) p with s = 9 (bf16) or 11
+# (fp16) significand bits, so an output row moves by at most that times
+# max |v|.  Bound used: 4x that, plus 1e-5 for the order of fp32 sums; the
+# log-sum-exp agrees to fp32 rounding relative to its size.
+_P_SPLIT = {"f16": 2.0 ** -22, "bf16": 2.0 ** -18, "i8": 0.0}
+
+
+def assert_paths_agree(out_a, out_b, lse_a, lse_b, kv_dtype, vmax):
+    tol_out = 1e-5 + 4 * _P_SPLIT[kv_dtype] * float(vmax)
+    d_out = (out_a - out_b).abs().max().item()
+    assert d_out <= tol_out, f"out differs by {d_out:.3e} > {tol_out:.3e}"
+    if lse_a is not None:
+        fin = torch.isfinite(lse_a) & torch.isfinite(lse_b)
+        assert torch.equal(torch.isfinite(lse_a), torch.isfinite(lse_b))
+        if fin.any():
+            d = (lse_a[fin] - lse_b[fin]).abs()
+            tol = 2e-6 * lse_a[fin].abs().clamp(min=1.0)
+            assert bool((d <= tol).all()), f"lse differs by {d.max().item():.3e}"
+
 
 def run_step(inp, selector=None, n_sel_pages=None, fused=True, rebuild=True, bufs=None):
     """Metadata rebuild, then select + attend on the GPU; returns host copies."""

@@ -15,7 +15,8 @@ from oracle import decode, quest, sketch as osk
 from synth import get_workload, make_inputs, scaled
 
 from conftest import oracle_inputs, oracle_params, to_numpy
-from gpu_helpers import TOL_OUT, check_unit, gpu_selection, run_step, unswizzle_meta_row
+from gpu_helpers import (TOL_OUT, assert_paths_agree, check_unit, gpu_selection, run_step,
+                         unswizzle_meta_row)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,8 +69,7 @@ def test_separate_calls_equal_fused(name):
     _, b1, _ = run_step(inp, fused=True)
     _, b2, _ = run_step(inp, fused=False)
     assert torch.equal(b1.sel, b2.sel) and torch.equal(b1.sel_cnt, b2.sel_cnt)
-    assert (b1.out - b2.out).abs().max().item() <= 1e-5
-    assert (b1.lse - b2.lse).abs().max().item() <= 1e-5
+    assert_paths_agree(b1.out, b2.out, b1.lse, b2.lse, w.kv_dtype, inp.v_pool.float().abs().max())
 
 
 @pytest.mark.parametrize("name", ["tiny-ragged", "gqa-ragged", "sals-4x", "sals-6x-full-tail"])
@@ -149,7 +149,7 @@ def test_full_budget_sparse_equals_dense():
     spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, None, None, inp.page_table,
                                inp.seq_lens, d.out, d.lse, d.ws)
     assert gpu_selection(bufs, 0, 0) == list(range(49))
-    assert (bufs.out - d.out).abs().max().item() <= 1e-5
+    assert_paths_agree(bufs.out, d.out, bufs.lse, d.lse, w.kv_dtype, inp.v_pool.float().abs().max())
 
 
 @pytest.mark.parametrize("name", ["tiny-ragged", "mha", "gqa-ragged", "long-d64-g8"])
