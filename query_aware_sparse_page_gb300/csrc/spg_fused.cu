@@ -68,7 +68,7 @@ struct FusedArgs {
   int32_t* err;
   int Hkv, S, MP, n_phys, n_sink, n_recent, n_sel, stages, rows_per_stage, append;
   int cluster, pages_per_stage;
-  uint32_t stage_bytes, row_bytes, page_bytes, ring_bytes, keys_off, sel_off;
+  uint32_t stage_bytes, row_bytes, page_bytes, ring_bytes, keys_off, sel_off, att_off;
   float scale_log2, inv_sqrt_d;
 };
 
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   __shared__ float s_P[SEL ? 256 * 16 : 1];
   __shared__ int s_qc[4];
   __shared__ float s_sq;
-  __shared__ int s_count;
+  __shared__ int s_natt;  // pages of the selection this CTA attends to
 
   const int S = a.S, STAGES = a.stages, R = a.rows_per_stage, PPS = a.pages_per_stage;
   const uint32_t sbytes = a.stage_bytes, rb = a.row_bytes, pbytes = a.page_bytes;
@@ -146,6 +146,10 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + a.keys_off);       // leader: keys
   float* s_part = reinterpret_cast<float*>(smem + a.keys_off);            // leader: partials
   int* s_sel = reinterpret_cast<int*>(smem + a.sel_off);                  // leader: selection
+  TopkShared& tk = *reinterpret_cast<TopkShared*>(ring);  // leader: top-k state (ring idle then)
+  uint32_t* s_mm = reinterpret_cast<uint32_t*>(smem + a.att_off);         // leader: [2][C*CW] key min/max
+  int* s_att_ph = reinterpret_cast<int*>(s_mm + 2 * kMaxCluster * CW);    // [n_sel] physical pages
+  int* s_att_nv = s_att_ph + a.n_sel;                                     // [n_sel] valid tokens
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   const int rows = lo + min(nc, static_cast<int>(rank + 1) * cpc) - c0;
   const int n_scan = (rows + R - 1) / R;
   const uint32_t keys_leader = map_rank(s_keys, 0);
+  const uint32_t mm_leader = map_rank(s_mm, 0);
   bool ok = true;
 
   if (warp == CW) {
@@ -226,6 +231,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
     }
   } else {
     // consumers
+    uint32_t kmn = 0xffffffffu, kmx = 0u;  // of the keys this warp produces
     if constexpr (SEL == 0) {
       QuestMma<T, D, G> qm;
       qm.init(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D, lane);
@@ -244,9 +250,18 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
           qm.tile(st + ti * 16 * 2 * D, pt0, lane, s0, s1);
           if ((lane & 3) == 0) {
             const int g = lane >> 2;
-            if (ti * 16 + g < nr) st_cluster_u32(keys_leader + 4u * (pt0 + g - lo), score_key(s0));
-            if (ti * 16 + g + 8 < nr)
-              st_cluster_u32(keys_leader + 4u * (pt0 + g + 8 - lo), score_key(s1));
+            if (ti * 16 + g < nr) {
+              const uint32_t k0 = score_key(s0);
+              st_cluster_u32(keys_leader + 4u * (pt0 + g - lo), k0);
+              kmn = min(kmn, k0);
+              kmx = max(kmx, k0);
+            }
+            if (ti * 16 + g + 8 < nr) {
+              const uint32_t k1 = score_key(s1);
+              st_cluster_u32(keys_leader + 4u * (pt0 + g + 8 - lo), k1);
+              kmn = min(kmn, k1);
+              kmx = max(kmx, k1);
+            }
           }
         }
         __syncwarp();
@@ -304,14 +319,25 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
           const float cz =
               __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r]), a.inv_sqrt_d);
           const float score = sketch_block_score(wk, S, qc, cz);
-          if (lane == 0) st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r - lo), score_key(score));
+          if (lane == 0) {
+            const uint32_t k0 = score_key(score);
+            st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r - lo), k0);
+            kmn = min(kmn, k0);
+            kmx = max(kmx, k0);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
       }
     }
+    kmn = __reduce_min_sync(0xffffffffu, kmn);
+    kmx = __reduce_max_sync(0xffffffffu, kmx);
+    if (lane == 0) {
+      st_cluster_u32(mm_leader + 4u * (rank * CW + warp), kmn);
+      st_cluster_u32(mm_leader + 4u * (kMaxCluster * CW + rank * CW + warp), kmx);
+    }
   }
-  cluster_sync();  // every key is in the leader
+  cluster_sync();  // every key (and every warp's key min / max) is in the leader
 
   // ------------------------------------------------------------- selection
   if (rank == 0) {
@@ -324,34 +350,31 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
     if (k_top == nc) {
       for (int i = tid; i < nc; i += nt) s_sel[lo + i] = lo + i;
     } else if (k_top > 0) {
-      block_topk(s_keys, nc, k_top, lo, s_sel + lo, *reinterpret_cast<TopkShared*>(ring));
+      for (int i = tid; i < 512; i += nt) reinterpret_cast<int4*>(tk.hist)[i] = make_int4(0, 0, 0, 0);
+      if (warp == 0) {  // the keys' min / max, from the scanning warps' reports
+        uint32_t kn = lane < C * CW ? s_mm[lane] : 0xffffffffu;
+        uint32_t kx = lane < C * CW ? s_mm[kMaxCluster * CW + lane] : 0u;
+        kn = __reduce_min_sync(0xffffffffu, kn);
+        kx = __reduce_max_sync(0xffffffffu, kx);
+        if (lane == 0) {
+          tk.kmin = kn;
+          tk.kmax = kx;
+        }
+      }
+      __syncthreads();
+      block_topk(s_keys, nc, k_top, lo, s_sel + lo, tk, true, true);
     }
-    if (tid == 0) s_count = count;
     __syncthreads();
+    // the selection to HBM, and each CTA's slice of it (physical page, valid
+    // tokens) into that CTA's shared memory, so that its attend phase starts
+    // from local data
     int32_t* gsel = a.sel + static_cast<size_t>(unit) * a.n_sel;
-    for (int i = tid; i < a.n_sel; i += nt) gsel[i] = i < count ? s_sel[i] : -1;
-    if (tid == 0) a.sel_cnt[unit] = count;
-  }
-  cluster_sync();  // the selection is in the leader
-
-  // ---------------------------------------------------------------- attend
-  const int count = ld_cluster_s32(map_rank(&s_count, 0));
-  const int ppc = (count + C - 1) / C;
-  const int a0 = min(count, static_cast<int>(rank) * ppc);
-  const int n_att = min(count, a0 + ppc) - a0;
-  Consumer cons;
-  if (warp == CW) {
-    const uint32_t sel_leader = map_rank(s_sel, 0);
-    const T* kpool = static_cast<const T*>(a.k_pool);
-    const T* vpool = static_cast<const T*>(a.v_pool);
-    const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
-    const uint32_t scb = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
-    const uint64_t pol = policy_evict_first();
-    for (int base = 0; base < n_att && ok; base += 32) {
-      int ph = -1, nv = 0;
-      const int j = base + lane;
-      if (j < n_att) {
-        const int lp = ld_cluster_s32(sel_leader + 4u * (a0 + j));
+    const int ppc = (count + C - 1) / C;
+    for (int i = tid; i < a.n_sel; i += nt) {
+      const int lp = i < count ? s_sel[i] : -1;
+      gsel[i] = lp;
+      if (i < count) {
+        int ph = -1, nv = 0;
         if (lp < 0 || lp >= P) {
           record_error(a.err, SPG_DEVERR_SEL);
         } else {
@@ -363,6 +386,34 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
             nv = min(S, L - lp * S);
           }
         }
+        const uint32_t r = static_cast<uint32_t>(i / ppc), j = static_cast<uint32_t>(i - r * ppc);
+        st_cluster_u32(map_rank(s_att_ph + j, r), static_cast<uint32_t>(ph));
+        st_cluster_u32(map_rank(s_att_nv + j, r), static_cast<uint32_t>(nv));
+      }
+    }
+    if (tid < C) {
+      const int na = min(count, (tid + 1) * ppc) - min(count, tid * ppc);
+      st_cluster_u32(map_rank(&s_natt, static_cast<uint32_t>(tid)), static_cast<uint32_t>(na));
+    }
+    if (tid == 0) a.sel_cnt[unit] = count;
+  }
+  cluster_sync();  // every CTA has its slice of the selection
+
+  // ---------------------------------------------------------------- attend
+  const int n_att = s_natt;
+  Consumer cons;
+  if (warp == CW) {
+    const T* kpool = static_cast<const T*>(a.k_pool);
+    const T* vpool = static_cast<const T*>(a.v_pool);
+    const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
+    const uint32_t scb = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
+    const uint64_t pol = policy_evict_first();
+    for (int base = 0; base < n_att && ok; base += 32) {
+      int ph = -1, nv = 0;
+      const int j = base + lane;
+      if (j < n_att) {
+        ph = s_att_ph[j];
+        nv = s_att_nv[j];
       }
       // one stage at a time: PPS pages, one lane each
       const int nb = min(32, n_att - base);
@@ -506,7 +557,10 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   const size_t keys_bytes =
       max(sizeof(uint32_t) * p.max_pages_per_seq, sizeof(float) * kMaxCluster * G * (D + 2));
   const size_t sel_off = (keys_off + keys_bytes + 127) & ~static_cast<size_t>(127);
-  const size_t smem = 1024 + sel_off + sizeof(int) * n_sel_pages(p);  // + alignment slack
+  const size_t att_off = (sel_off + sizeof(int) * n_sel_pages(p) + 127) & ~static_cast<size_t>(127);
+  const size_t att_bytes = sizeof(uint32_t) * 2 * kMaxCluster * kConsumerWarps +
+                           sizeof(int) * 2 * n_sel_pages(p);
+  const size_t smem = 1024 + att_off + att_bytes;  // + alignment slack
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
   if constexpr (!is_i8<T>()) {
     const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
@@ -523,6 +577,7 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   a.ring_bytes = static_cast<uint32_t>(ring);
   a.keys_off = static_cast<uint32_t>(keys_off);
   a.sel_off = static_cast<uint32_t>(sel_off);
+  a.att_off = static_cast<uint32_t>(att_off);
 
   auto kern = k_fused<T, TQ, D, G, 1>;  // int8 pools are only scored by the sketch selector
   if constexpr (!is_i8<T>())
@@ -545,15 +600,21 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  // Load-balancing cluster placement: with the next step's CTAs launched
+  // early (programmatic serialisation) the default placement can leave a
+  // GPC's free slots too scattered for a whole cluster, and that cluster then
+  // runs after the others, a full step late.
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[2].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  attr[2].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 3;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

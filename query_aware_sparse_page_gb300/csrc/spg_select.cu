@@ -55,8 +55,9 @@ struct SelectArgs {
 // Selection of one unit from its scores row (global, written by this launch
 // or the previous one): forced sinks, the exact top-k candidates, forced
 // recent pages, then -1 padding; sel_cnt.
+template <int MAXN>
 __device__ void select_unit(const float* srow, int P, int lo, int hi, int n_sel, int32_t* out,
-                            int32_t* cnt_out, uint32_t* s_keys, TopkShared& t) {
+                            int32_t* cnt_out, uint32_t* s_keys, TopkSmem<MAXN>& t) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int nc = hi - lo, nf = P - nc;
   const int k_top = min(max(n_sel - nf, 0), nc);
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(128) k_quest_select(const SelectArgs a, int fu
 template <typename TQ>
 __global__ void __launch_bounds__(256) k_sketch_select(const SelectArgs a, int fused) {
   constexpr int DS = 16;
-  extern __shared__ uint32_t s_keys[];
+  extern __shared__ __align__(128) uint32_t s_keys[];  // 16-byte key loads
   __shared__ float s_qbar[256];
   __shared__ float s_P[256 * DS];
   __shared__ int s_qc[4];  // packed int8 codes: even 0-6, odd 1-7, even 8-14, odd 9-15
@@ -208,8 +209,8 @@ __global__ void __launch_bounds__(256) k_sketch_select(const SelectArgs a, int f
 // Selection alone, for page tables too long to select inside the scoring
 // launch: one CTA (1024 threads) per (batch, kv-head).
 __global__ void __launch_bounds__(1024) k_topk(const SelectArgs a) {
-  extern __shared__ uint32_t s_keys[];
-  __shared__ TopkShared s_t;
+  extern __shared__ __align__(128) uint32_t s_keys[];  // 16-byte key loads
+  __shared__ TopkSmem<kMaxTopkPages> s_t;
   pdl_wait();
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv;

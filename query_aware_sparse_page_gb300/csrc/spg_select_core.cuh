@@ -68,121 +68,345 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_t
   return r;
 }
 
-struct TopkShared {
+// Shared state of the block top-k for up to MAXN keys.
+#ifdef SPG_TOPK_PROFILE
+__device__ int g_topk_stop;
+#define SPG_TK_MARK(t, i) \
+  do {                    \
+    if (threadIdx.x == 0) (t).marks[i] = clock64(); \
+    if (g_topk_stop == (i)) { __syncthreads(); return; } \
+  } while (0)
+#else
+#define SPG_TK_MARK(t, i) \
+  do {                    \
+  } while (0)
+#endif
+
+// 16-byte aligned: the histogram is cleared and read with 16-byte accesses
+template <int MAXN>
+struct alignas(16) TopkSmem {
+  static constexpr int kWords = (MAXN + 31) / 32;
   int hist[2048];
-  int warp_tot[32];
-  int total;
-  int digit, need, cnt;
-  uint32_t kmin, kmax;
+  int wa[32], wb[32];
+  int total, digit, need, cnt;
+  uint32_t kmin, kmax;  // min / max of the keys (set by the caller when it knows them)
+  uint32_t thr;         // exact threshold key found among the candidates
+  int need_thr;         // keys equal to thr to take, lowest indices first
+  int ncand;
+  int cand[256];        // indices of the keys in the threshold bucket, when it is small
+  uint32_t candk[256];  // and their keys
+  uint32_t gtw[kWords];  // bitmap: keys above the threshold
+  uint32_t eqw[kWords];  // bitmap: keys in the threshold bucket (or equal to the threshold)
+#ifdef SPG_TOPK_PROFILE
+  long long marks[8];
+  long long fb[3];
+  int fb_rounds;
+#endif
 };
 
-// Exact top-k of keys[0, n) (shared memory), larger key first, lower index
-// first among equal keys; writes the chosen indices + base, ascending, to
-// dst[0, k).  0 < k < n.  Every thread of the block calls it.
-inline __device__ void block_topk(const uint32_t* keys, int n, int k, int base, int32_t* dst,
-                           TopkShared& t) {
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  const int nw = nt >> 5;
-  uint32_t mn = 0xffffffffu, mx = 0u;
-  for (int i = tid; i < n; i += nt) {
-    const uint32_t x = keys[i];
-    mn = min(mn, x);
-    mx = max(mx, x);
+// Block-wide search of t.hist[0, 2048) (bins past the pass's bin count are
+// zero) for the bin in which the descending cumulative count reaches `need`:
+// t.digit, t.need (still needed inside it), t.cnt (its keys).  Thread j < 128
+// holds bins [2048 - 16 (j + 1), 2048 - 16 j) in registers (four 16-byte
+// loads); one block scan of the per-thread sums finds the thread, which then
+// walks its registers.  Every thread calls it.
+template <int MAXN>
+__device__ __forceinline__ void topk_find_bin(TopkSmem<MAXN>& t, int need) {
+  const int tid = threadIdx.x;
+  int4 q[4] = {};
+  int sum = 0;
+  if (tid < 128) {
+    const int4* h4 = reinterpret_cast<const int4*>(t.hist);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) q[u] = h4[511 - 4 * tid - u];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sum += q[u].x + q[u].y + q[u].z + q[u].w;
   }
-  mn = __reduce_min_sync(0xffffffffu, mn);
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) {
-    t.hist[warp] = static_cast<int>(mn);
-    t.hist[32 + warp] = static_cast<int>(mx);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t a = lane < nw ? static_cast<uint32_t>(t.hist[lane]) : 0xffffffffu;
-    uint32_t c = lane < nw ? static_cast<uint32_t>(t.hist[32 + lane]) : 0u;
-    a = __reduce_min_sync(0xffffffffu, a);
-    c = __reduce_max_sync(0xffffffffu, c);
-    if (lane == 0) {
-      t.kmin = a;
-      t.kmax = c;
+  const int excl = block_exclusive_scan(sum, t.wa, &t.total);
+  if (tid < 128 && excl < need && excl + sum >= need) {
+    int acc = excl;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v[4] = {q[u].w, q[u].z, q[u].y, q[u].x};  // descending bins
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (acc < need && acc + v[e] >= need) {
+          t.digit = 2047 - 16 * tid - 4 * u - e;
+          t.need = need - acc;
+          t.cnt = v[e];
+        }
+        acc += v[e];
+      }
     }
   }
   __syncthreads();
-  mn = t.kmin;
-  mx = t.kmax;
+}
+
+// Chunk u of a run of 16-byte chunks, visited in an order rotated by `rot`:
+// threads whose runs start at the same offset modulo 128 bytes but differ in
+// `rot` then hit different bank groups on each load.  The caller does not
+// depend on the order (or shifts results by the chunk index).
+__device__ __forceinline__ uint4 rot_chunk(const uint32_t* p, int u, int rot, int nchunks, int& j) {
+  j = (u + rot) & (nchunks - 1);
+  return reinterpret_cast<const uint4*>(p)[j];
+}
+
+// Exact top-k of keys[0, n) (shared memory, 16-byte aligned, n <= MAXN):
+// larger key first, lower index first among equal keys; writes the chosen
+// indices + base, ascending, to dst[0, k).  0 < k < n; blockDim.x >= 128.
+// Every thread of the block calls it.  minmax_ready: the caller has stored
+// the keys' min / max in t.kmin / t.kmax; hist_clear: t.hist is already all
+// zeros (both made visible by a barrier).
+//
+// Radix selection on the order-preserving keys: the bits every key shares
+// are skipped and a histogram pass resolves the next 11 bits, as often as it
+// takes for the bucket holding the k-th key to be taken whole or to hold at
+// most 256 keys.  One pass then records, as bitmaps (a thread per 32 keys),
+// the keys above that bucket and the keys in it, gathering the latter when
+// there are few; the exact threshold among the gathered keys is found by
+// counting, for each, the keys above and equal to it, and the bitmaps are
+// corrected.  Warp 0 turns the bitmaps into ascending indices: every key
+// above, plus the first `need` keys equal to the threshold.
+template <int MAXN>
+__device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, int n, int k,
+                                           int base, int32_t* __restrict__ dst, TopkSmem<MAXN>& t,
+                                           bool minmax_ready = false, bool hist_clear = false) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = nt >> 5;
+  const int n16 = n & ~15;  // keys in whole 16-key runs; the tail is read one by one
+  SPG_TK_MARK(t, 0);
+  if (!minmax_ready) {
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (int r = tid; r * 16 < n16; r += nt) {  // runs 64 B apart: rotate by r / 2
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        int j;
+        const uint4 v = rot_chunk(keys + r * 16, u, r >> 1, 4, j);
+        mn = min(min(mn, min(v.x, v.y)), min(v.z, v.w));
+        mx = max(max(mx, max(v.x, v.y)), max(v.z, v.w));
+      }
+    }
+    for (int i = n16 + tid; i < n; i += nt) {
+      mn = min(mn, keys[i]);
+      mx = max(mx, keys[i]);
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+      t.wa[warp] = static_cast<int>(mn);
+      t.wb[warp] = static_cast<int>(mx);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t a = lane < nw ? static_cast<uint32_t>(t.wa[lane]) : 0xffffffffu;
+      uint32_t c = lane < nw ? static_cast<uint32_t>(t.wb[lane]) : 0u;
+      a = __reduce_min_sync(0xffffffffu, a);
+      c = __reduce_max_sync(0xffffffffu, c);
+      if (lane == 0) {
+        t.kmin = a;
+        t.kmax = c;
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t mn = t.kmin, mx = t.kmax;
   uint32_t prefix, mask;
   int need = k;
+  bool resolve = false;
   if (mn == mx) {  // every key equal: the lowest indices win
     prefix = mx;
     mask = 0xffffffffu;
   } else {
     int hb = 31 - __clz(static_cast<int>(mn ^ mx));  // highest bit where keys differ
-    mask = ~((2u << hb) - 1u);                         // the bits every key shares
+    mask = hb == 31 ? 0u : ~((2u << hb) - 1u);         // the bits every key shares
     prefix = mx & mask;
+    bool first = true;
     while (true) {
       const int shift = max(hb - 10, 0);
-      const int bins = 1 << (hb - shift + 1);
-      for (int i = tid; i < bins; i += nt) t.hist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < n; i += nt) {
-        const uint32_t x = keys[i];
-        if ((x & mask) == prefix) atomicAdd(&t.hist[(x >> shift) & (bins - 1)], 1);
+      const int nb = 1 << (hb - shift + 1);
+      if (!(first && hist_clear)) {
+        for (int i = tid; i < 512; i += nt) reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
+        __syncthreads();
       }
-      __syncthreads();
-      // bins in descending order, a contiguous run per thread
-      const int bpt = (bins + nt - 1) / nt;
-      const int top = bins - 1 - tid * bpt;
-      int local = 0;
-      for (int j = 0; j < bpt; ++j)
-        if (top - j >= 0) local += t.hist[top - j];
-      const int excl = block_exclusive_scan(local, t.warp_tot, &t.total);
-      if (excl < need && excl + local >= need) {
-        int acc = excl;
-        for (int j = 0; j < bpt; ++j) {
-          const int c = t.hist[top - j];
-          if (acc + c >= need) {
-            t.digit = top - j;
-            t.need = need - acc;
-            t.cnt = c;
-            break;
-          }
-          acc += c;
+      SPG_TK_MARK(t, 1);
+      for (int r = tid; r * 16 < n16; r += nt) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          int j;
+          v[u] = rot_chunk(keys + r * 16, u, r >> 1, 4, j);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (first || (x[e] & mask) == prefix) atomicAdd(&t.hist[(x[e] >> shift) & (nb - 1)], 1);
         }
       }
+      for (int i = n16 + tid; i < n; i += nt) {
+        const uint32_t x = keys[i];
+        if (first || (x & mask) == prefix) atomicAdd(&t.hist[(x >> shift) & (nb - 1)], 1);
+      }
       __syncthreads();
-      const int digit = t.digit, cnt = t.cnt;
+      SPG_TK_MARK(t, 2);
+      topk_find_bin(t, need);
+      SPG_TK_MARK(t, 3);
+      first = false;
+      const int cnt = t.cnt;
+      prefix |= static_cast<uint32_t>(t.digit) << shift;
+      mask |= static_cast<uint32_t>(nb - 1) << shift;
       need = t.need;
-      prefix |= static_cast<uint32_t>(digit) << shift;
-      mask |= static_cast<uint32_t>(bins - 1) << shift;
-      __syncthreads();
       if (cnt == need || shift == 0) break;  // the whole bucket is taken, or keys are exact
+      if (cnt <= 256) {
+        resolve = true;
+        break;
+      }
       hb = shift - 1;
     }
   }
-  // compaction in index order: keys above the threshold bucket, plus the
-  // first `need` keys inside it
-  const int seg = (n + nt - 1) / nt;
-  const int i0 = min(tid * seg, n), i1 = min(i0 + seg, n);
-  int n_eq = 0, n_gt = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t x = keys[i] & mask;
-    n_eq += (x == prefix);
-    n_gt += (x > prefix);
-  }
-  const int eq_base = block_exclusive_scan(n_eq, t.warp_tot, &t.total);
-  const int eq_take = min(max(need - eq_base, 0), n_eq);
-  int pos = block_exclusive_scan(n_gt + eq_take, t.warp_tot, &t.total);
-  int r = eq_base;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t x = keys[i] & mask;
-    bool take = x > prefix;
-    if (x == prefix) {
-      take = r < need;
-      ++r;
+  SPG_TK_MARK(t, 4);
+  // bitmaps of the keys above the bucket / in it: thread per 32-key word
+  const int W = (n + 31) >> 5;
+  if (tid == 0) t.ncand = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < W; c0 += nt) {  // block-uniform rounds (warp-level slot allocation)
+    const int c = c0 + tid;
+    uint32_t bg = 0u, be = 0u;
+    if (c < W) {
+      const int i0 = c << 5;
+      if (i0 + 32 <= n16) {  // words 128 B apart: rotate over the 8 chunks
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          int j;
+          const uint4 v = rot_chunk(keys + i0, u, c, 8, j);
+          const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t xm = x[e] & mask;
+            bg |= static_cast<uint32_t>(xm > prefix) << (4 * j + e);
+            be |= static_cast<uint32_t>(xm == prefix) << (4 * j + e);
+          }
+        }
+      } else {
+        for (int j = 0; j < 32 && i0 + j < n; ++j) {
+          const uint32_t xm = keys[i0 + j] & mask;
+          bg |= static_cast<uint32_t>(xm > prefix) << j;
+          be |= static_cast<uint32_t>(xm == prefix) << j;
+        }
+      }
+      t.gtw[c] = bg;
+      t.eqw[c] = be;
     }
-    if (take) dst[pos++] = base + i;
+    if (resolve) {
+      // candidate slots: one atomic per warp
+      const int m = __popc(be);
+      int incl = m;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int wbase = 0;
+      if (lane == 31) wbase = atomicAdd(&t.ncand, incl);
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      int slot = wbase + incl - m;
+      uint32_t e = be;
+      while (e) {
+        const int j = __ffs(e) - 1;
+        e &= e - 1u;
+        t.cand[slot] = (c << 5) + j;
+        t.candk[slot] = keys[(c << 5) + j];
+        ++slot;
+      }
+    }
   }
+  __syncthreads();
+  SPG_TK_MARK(t, 5);
+  if (resolve) {
+    // exact threshold among the bucket's keys (cnt <= 256)
+    const int cnt = t.ncand;
+    for (int q = tid; q < cnt; q += nt) {
+      const uint32_t x = t.candk[q];
+      int gt = 0, eq = 0;
+#pragma unroll 8
+      for (int j = 0; j < cnt; ++j) {
+        const uint32_t y = t.candk[j];
+        gt += y > x;
+        eq += y == x;
+      }
+      if (gt < need && need <= gt + eq) {  // x is the need-th largest (every such x is equal)
+        t.thr = x;
+        t.need_thr = need - gt;
+      }
+    }
+    __syncthreads();
+    const uint32_t thr = t.thr;
+    for (int q = tid; q < cnt; q += nt) {
+      const uint32_t x = t.candk[q];
+      const int ci = t.cand[q];
+      if (x != thr) {
+        const uint32_t bit = 1u << (ci & 31);
+        if (x > thr) atomicOr(&t.gtw[ci >> 5], bit);
+        atomicAnd(&t.eqw[ci >> 5], ~bit);
+      }
+    }
+    need = t.need_thr;
+    __syncthreads();
+  }
+  SPG_TK_MARK(t, 6);
+  // warp 0: words -> ascending indices (lane L owns words [L*wpl, (L+1)*wpl)).
+  // Keys equal to the threshold are taken in index order, so the number taken
+  // before a lane is min(equal keys before it, need).
+  if (warp == 0) {
+    const int wpl = (W + 31) / 32;
+    const int c0 = min(W, lane * wpl), c1 = min(W, c0 + wpl);
+    int e_loc = 0, g_loc = 0;
+    for (int c = c0; c < c1; ++c) {
+      e_loc += __popc(t.eqw[c]);
+      g_loc += __popc(t.gtw[c]);
+    }
+    int e_incl = e_loc, g_incl = g_loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ve = __shfl_up_sync(0xffffffffu, e_incl, o);
+      const int vg = __shfl_up_sync(0xffffffffu, g_incl, o);
+      if (lane >= o) {
+        e_incl += ve;
+        g_incl += vg;
+      }
+    }
+    int e_seen = e_incl - e_loc;
+    int pos = (g_incl - g_loc) + min(e_seen, need);
+    for (int c = c0; c < c1; ++c) {
+      uint32_t e = t.eqw[c];
+      const uint32_t g = t.gtw[c];
+      const int pe = __popc(e);
+      if (e_seen >= need) {
+        e = 0u;
+      } else if (e_seen + pe > need) {  // keep the lowest need - e_seen set bits
+        uint32_t keep = 0u;
+        for (int r = need - e_seen; r > 0; --r) {
+          keep |= e & (~e + 1u);
+          e &= e - 1u;
+        }
+        e = keep;
+      }
+      e_seen += pe;
+      uint32_t f = e | g;
+      while (f) {
+        dst[pos++] = base + (c << 5) + (__ffs(f) - 1);
+        f &= f - 1u;
+      }
+    }
+  }
+  __syncthreads();
+  SPG_TK_MARK(t, 7);
 }
 
+using TopkShared = TopkSmem<8192>;
+static_assert(alignof(TopkShared) >= 16 && alignof(TopkSmem<kMaxTopkPages>) >= 16,
+              "16-byte accesses to the histogram");
 
 // Quest bound of one page for the group's G query rows: a half-warp holds
 // CPL = D/16 channels of the row per lane (wm / wM: m and M as packed
