@@ -37,6 +37,37 @@ NOMINAL_HBM_GBS = 8000.0
 
 
 # ---------------------------------------------------------------------------- utils
+# DRAM bytes (read + write) of one k_fused launch, from one ncu capture of
+# that workload, and the sha256 of the kernel sources it was taken on
+# (profiles/k_fused_<workload>.md).  Reported only while the sources match.
+NCU_TRAFFIC = {
+    "llama2-7b-mha-32k": (67_919_360, "ca081df70fc8e95b575012a49c8438d4460d57e4d640849292c8fc1e62fe00e5"),
+    "long-scan-b4-128k": (205_535_232, "ca081df70fc8e95b575012a49c8438d4460d57e4d640849292c8fc1e62fe00e5"),
+}
+
+
+def csrc_sha256() -> str:
+    import hashlib
+
+    d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "query_aware_sparse_page_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str):
+    rec = NCU_TRAFFIC.get(workload)
+    if rec is None:
+        return None, "no ncu capture of this workload"
+    if rec[1] != csrc_sha256():
+        return None, "kernel sources changed since the ncu capture"
+    return rec[0], f"profiles/k_fused_{workload}.md"
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -318,6 +349,7 @@ def run_ours(args, world, rank, local):
     kname, dom_ms, dom_bytes = "k_fused", ms_step, total_b
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else 0.0
 
+    traffic, traffic_src = ncu_traffic(w.name)
     e2e = run_e2e(args, spg, layers, stream, world, dev)
     launches_per_step = 1 if (w.selector == "quest" and w.max_pages_per_seq <= 8192) else 2
 
@@ -375,7 +407,8 @@ def run_ours(args, world, rank, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_kind": peak_kind,
-            "traffic": None,
+            "traffic": traffic,
+            "traffic_source": traffic_src,
             "algorithmic_bytes": dom_bytes,
             "ms_per_launch": round(float(dom_ms), 5),
         },
