@@ -9,23 +9,30 @@
 // SequenceO1 close reading §2.4 / §3.3 (fusing selection and attention: the
 // indices never leave the chip here, they cross shared memory).
 //
-// Phases of one cluster (every CTA has 4 consumer warps and 1 producer warp):
+// Phases of one cluster (every CTA has 4 consumer warps, 1 producer warp and
+// 1 auxiliary warp;
+// each ring stage has one owner warp, stage k belonging to warp k % 4):
 //  1. scan: the unit's candidate pages are split into contiguous chunks, one
 //     per CTA.  Metadata is stored per sequence in logical page order, so a
 //     chunk's rows (Quest: m and M, 2*d elements; sketch: the block's int4
 //     codes) are one contiguous range; the producer streams it into the
-//     shared-memory ring with one cp.async.bulk per stage of up to 64 rows,
-//     and the consumers score each row and store its
-//     order-preserving key straight into the leader CTA's shared memory
-//     (distributed shared memory, st.shared::cluster).
+//     shared-memory ring with one cp.async.bulk per stage of up to 64 rows.
+//     Quest rows are scored 16 pages per tensor-core tile (A = the rows,
+//     B = [q-; q+] for the group's query rows), sketch blocks by int8 dots.
+//     Each order-preserving key goes straight into the leader CTA's shared
+//     memory (st.shared::cluster), and each warp reports its keys' min / max.
 //  2. cluster barrier; the leader (rank 0) runs the exact top-k over the
-//     keys, adds the forced pages and writes sel / sel_cnt; cluster barrier.
-//  3. attend: each CTA takes a contiguous slice of the selection (read from
-//     the leader's shared memory), streams those pages' K/V tiles through the
-//     same ring (TMA bulk copies, page-table lookup by the producer) and runs
-//     the online-softmax consumer; the CTA's partial (m, l, acc) per query row
-//     goes into the leader's shared memory.
-//  4. cluster barrier; the leader merges the 8 partials and writes out / lse.
+//     keys, adds the forced pages, writes sel / sel_cnt, and pushes each
+//     CTA's slice of the selection (physical page, valid tokens) into that
+//     CTA's shared memory; cluster barrier.
+//  3. attend: each CTA's producer copies its pages' K/V tiles into the ring
+//     (fp16/bf16: 2-D TMA tiles with 128-byte swizzle for the tensor-core
+//     consumer; int8: bulk copies with their scales for the CUDA-core
+//     consumer); the CTA's partial (m, l, acc) per query row goes into the
+//     leader's shared memory.
+//  4. cluster barrier; the leader merges the partials and writes out / lse.
+// An auxiliary warp of the last CTA applies the Quest append of the new token
+// during the scan (that token's page is forced, so nothing reads its row).
 // No CTA waits on another except at the three hardware cluster barriers,
 // which every thread of every CTA reaches on every path; all mbarrier waits
 // are bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still
@@ -119,7 +126,7 @@ __device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int 
 }
 
 template <typename T, typename TQ, int D, int G, int SEL>
-__global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
+__global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     k_fused(const __grid_constant__ FusedArgs a) {
   constexpr int CW = kConsumerWarps;
   constexpr bool MMA = !is_i8<T>();  // tensor-core consumer, TMA tile producer
@@ -182,11 +189,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo), nc = hi - lo;
   __syncthreads();
 
-  if constexpr (SEL == 0) {
-    // the appended token's page is forced (n_recent >= 1): no CTA scans it
-    if (a.append && rank == C - 1 && warp == 0 && L > 0) append_minmax_warp<T, D>(a, b, h, L, lane);
-  }
-
   // ------------------------------------------------------------------ scan
   const int cpc = (nc + C - 1) / C;
   const int c0 = lo + min(nc, static_cast<int>(rank) * cpc);
@@ -229,6 +231,12 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[stage]);
     }
+  } else if (warp == CW + 1) {
+    // auxiliary warp: the Quest append of the token at L-1.  Its page is
+    // forced (n_recent >= 1), so neither this step's scan nor its attend
+    // reads that metadata row; done here it overlaps the scan.
+    if constexpr (SEL == 0)
+      if (a.append && rank == C - 1 && L > 0) append_minmax_warp<T, D>(a, b, h, L, lane);
   } else {
     // consumers
     uint32_t kmn = 0xffffffffu, kmx = 0u;  // of the keys this warp produces
@@ -462,7 +470,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
       for (int k = max(0, issued - STAGES); k < issued; ++k)
         mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
     }
-  } else {
+  } else if (warp < CW) {
     cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
               a.scale_log2, warp, lane);
     const int n_att_st = (n_att + PPS - 1) / PPS;
@@ -531,7 +539,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
 
 template <typename T, typename TQ, int D, int G>
 cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
-  constexpr int threads = (kConsumerWarps + 1) * 32;
+  constexpr int threads = (kConsumerWarps + 2) * 32;  // + producer + auxiliary warp
   const int S = p.page_size;
   const uint32_t pb = kv_stage_bytes<T, D>(S);
   const uint32_t rb = p.selector == SPG_SEL_QUEST ? 2u * D * sizeof(T) : static_cast<uint32_t>(S) * 8u;
