@@ -40,7 +40,36 @@ __device__ __forceinline__ void load_row_chunk(const T* p, uint32_t (&w)[CPL / 2
   }
 }
 
-// ---- block-wide exclusive scan of one int per thread -----------------------
+// ---- block-wide exclusive scan of one value per thread (int, or uint32
+// with wrap-around addition) -----------------------------------------------
+template <typename V>
+__device__ __forceinline__ V block_exclusive_scan_t(V v, V* s_warp, V* s_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  V incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const V n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    V w = lane < nw ? s_warp[lane] : V(0);
+    V wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const V n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) s_warp[lane] = wi - w;
+    if (lane == 31) *s_total = wi;
+  }
+  __syncthreads();
+  const V r = s_warp[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int incl = v;
@@ -266,40 +295,62 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     }
   }
   SPG_TK_MARK(t, 4);
-  // bitmaps of the keys above the bucket / in it: thread per 32-key word
+  // bitmaps of the keys above the bucket / in it: four threads per 32-key
+  // word (8 keys each), two words per quad per round, OR-combined with two
+  // shuffles
   const int W = (n + 31) >> 5;
-  if (tid == 0) t.ncand = 0;
-  __syncthreads();
-  for (int c0 = 0; c0 < W; c0 += nt) {  // block-uniform rounds (warp-level slot allocation)
-    const int c = c0 + tid;
-    uint32_t bg = 0u, be = 0u;
-    if (c < W) {
-      const int i0 = c << 5;
-      if (i0 + 32 <= n16) {  // words 128 B apart: rotate over the 8 chunks
+  const int qd = tid >> 2, sub = tid & 3, wpr = nt >> 1;  // quad, its quarter of a word, words per round
+  for (int c0 = 0; c0 < W; c0 += wpr) {  // block-uniform rounds
+    uint32_t bg[2] = {0u, 0u}, be[2] = {0u, 0u};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          int j;
-          const uint4 v = rot_chunk(keys + i0, u, c, 8, j);
-          const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+    for (int h = 0; h < 2; ++h) {
+      const int c = c0 + 2 * qd + h;
+      if (c < W) {
+        const int i0 = (c << 5) + 8 * sub;
+        if ((c << 5) + 32 <= n16) {
+          // chunks 2 sub and 2 sub + 1 of the word, order flipped on odd
+          // words: the 8 threads of a quarter-warp hit 8 different bank groups
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t xm = x[e] & mask;
-            bg |= static_cast<uint32_t>(xm > prefix) << (4 * j + e);
-            be |= static_cast<uint32_t>(xm == prefix) << (4 * j + e);
+          for (int u = 0; u < 2; ++u) {
+            const int uu = u ^ (c & 1);
+            const uint4 v = reinterpret_cast<const uint4*>(keys + i0)[uu];
+            const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t xm = x[e] & mask;
+              bg[h] |= static_cast<uint32_t>(xm > prefix) << (8 * sub + 4 * uu + e);
+              be[h] |= static_cast<uint32_t>(xm == prefix) << (8 * sub + 4 * uu + e);
+            }
+          }
+        } else {
+          for (int j = 0; j < 8 && i0 + j < n; ++j) {
+            const uint32_t xm = keys[i0 + j] & mask;
+            bg[h] |= static_cast<uint32_t>(xm > prefix) << (8 * sub + j);
+            be[h] |= static_cast<uint32_t>(xm == prefix) << (8 * sub + j);
           }
         }
-      } else {
-        for (int j = 0; j < 32 && i0 + j < n; ++j) {
-          const uint32_t xm = keys[i0 + j] & mask;
-          bg |= static_cast<uint32_t>(xm > prefix) << j;
-          be |= static_cast<uint32_t>(xm == prefix) << j;
-        }
       }
-      t.gtw[c] = bg;
-      t.eqw[c] = be;
     }
-    if (resolve) {
-      // candidate slots: one atomic per warp
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      bg[h] |= __shfl_xor_sync(0xffffffffu, bg[h], 1);
+      be[h] |= __shfl_xor_sync(0xffffffffu, be[h], 1);
+      bg[h] |= __shfl_xor_sync(0xffffffffu, bg[h], 2);
+      be[h] |= __shfl_xor_sync(0xffffffffu, be[h], 2);
+      const int c = c0 + 2 * qd + h;
+      if (c < W && sub == 0) {
+        t.gtw[c] = bg[h];
+        t.eqw[c] = be[h];
+      }
+    }
+  }
+  if (resolve) {
+    // gather the bucket's keys (at most 256) from the non-zero bucket words
+    if (tid == 0) t.ncand = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < W; c0 += nt) {  // block-uniform rounds (one atomic per warp)
+      const int c = c0 + tid;
+      const uint32_t be = c < W ? t.eqw[c] : 0u;
       const int m = __popc(be);
       int incl = m;
 #pragma unroll
@@ -308,7 +359,7 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
         if (lane >= o) incl += v;
       }
       int wbase = 0;
-      if (lane == 31) wbase = atomicAdd(&t.ncand, incl);
+      if (lane == 31 && incl > 0) wbase = atomicAdd(&t.ncand, incl);
       wbase = __shfl_sync(0xffffffffu, wbase, 31);
       int slot = wbase + incl - m;
       uint32_t e = be;
@@ -355,29 +406,24 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     __syncthreads();
   }
   SPG_TK_MARK(t, 6);
-  // warp 0: words -> ascending indices (lane L owns words [L*wpl, (L+1)*wpl)).
-  // Keys equal to the threshold are taken in index order, so the number taken
-  // before a lane is min(equal keys before it, need).
-  if (warp == 0) {
-    const int wpl = (W + 31) / 32;
-    const int c0 = min(W, lane * wpl), c1 = min(W, c0 + wpl);
+  // words -> ascending indices, thread j owning words [j*wpt, (j+1)*wpt).
+  // Keys equal to the threshold are taken in index order, so the number
+  // taken before a thread is min(equal keys before it, need).  One block
+  // scan carries both counts (equal keys in the high half, keys above in the
+  // low half: each total is at most n < 65536).
+  {
+    const int wpt = (W + nt - 1) / nt;
+    const int c0 = min(W, tid * wpt), c1 = min(W, c0 + wpt);
     int e_loc = 0, g_loc = 0;
     for (int c = c0; c < c1; ++c) {
       e_loc += __popc(t.eqw[c]);
       g_loc += __popc(t.gtw[c]);
     }
-    int e_incl = e_loc, g_incl = g_loc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int ve = __shfl_up_sync(0xffffffffu, e_incl, o);
-      const int vg = __shfl_up_sync(0xffffffffu, g_incl, o);
-      if (lane >= o) {
-        e_incl += ve;
-        g_incl += vg;
-      }
-    }
-    int e_seen = e_incl - e_loc;
-    int pos = (g_incl - g_loc) + min(e_seen, need);
+    const uint32_t packed = block_exclusive_scan_t<uint32_t>(
+        (static_cast<uint32_t>(e_loc) << 16) | static_cast<uint32_t>(g_loc),
+        reinterpret_cast<uint32_t*>(t.wa), reinterpret_cast<uint32_t*>(&t.total));
+    int e_seen = static_cast<int>(packed >> 16);
+    int pos = static_cast<int>(packed & 0xffffu) + min(e_seen, need);
     for (int c = c0; c < c1; ++c) {
       uint32_t e = t.eqw[c];
       const uint32_t g = t.gtw[c];
