@@ -205,9 +205,10 @@ spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const
  * appended at seq_lens[b]-1 (as sparse_page_meta_update with rebuild == 0),
  * then sparse_decode_select_attend.  Where the parameters allow it (page
  * tables of at most 8192 pages), selection and attention run as one launch
- * of one 8-CTA thread-block cluster per (batch, kv-head), and for the Quest
- * selector with n_recent_pages >= 1 the append runs inside that launch too
- * (the appended token's page is forced, so no scoring depends on it). */
+ * of one 8-CTA thread-block cluster per (batch, kv-head); with
+ * n_recent_pages >= 1 (and sketch_dim 16 for the sketch selector) the append
+ * runs inside that launch too (the appended token's page is forced, so no
+ * scoring depends on it). */
 spg_status sparse_decode_step(const spg_params* p, const void* q, const void* k_pool,
                               const void* v_pool, const void* k_scale, const void* v_scale,
                               const int32_t* page_table, const int32_t* seq_lens, void* minmax,

@@ -365,6 +365,221 @@ struct AttnMma {
   }
 };
 
+// ---- tensor-core consumer for int8 pools ---------------------------------------
+// The same flash-decoding step for int8 K/V with fp16 per-token scales (SALS
+// SFAA: antiquant attention), fp16 query, D = 128.  int8 codes become fp16
+// exactly in registers: the byte biased to unsigned (x ^ 0x80) is placed
+// under an fp16 exponent byte 0x64 (the value 1024 + x + 128) and 1152 is
+// subtracted.  The staged page is the K tile [S rows][128 bytes] and the V
+// tile, each as left by a TMA tile copy with 128-byte swizzle (chunk c of row
+// r at chunk c ^ (r % 8)), then the S fp16 K scales and S fp16 V scales.
+//   S^T = K Q^T: ldmatrix on the int8 rows read as 16-bit pairs gives a lane
+//     4 consecutive channels 4q..4q+3 of one token (q = lane % 4) of a
+//     16-channel chunk; the k index of the mma is mapped to channels
+//     (2q, 2q+1 -> 4q, 4q+1; 2q+8, 2q+9 -> 4q+2, 4q+3), and the query's B
+//     fragments use the same map.  The logit of token t is multiplied by its
+//     K scale.
+//   O^T += V^T P'^T with p' = 256 p * (V scale of the token) (the power of
+//     two keeps small p' out of fp16's subnormal range; undone at the store):
+//     ldmatrix.trans on
+//     16-bit pairs gives a lane tokens (2q, 2q+1) x channels (2g, 2g+1); the
+//     m-tile's rows g and g + 8 are mapped to channels 2g and 2g + 1 of the
+//     chunk.
+template <int G>
+struct AttnMmaI8 {
+  static constexpr int D = 128;
+  static constexpr int NC = D / 16;  // 16-channel chunks: k-steps of Q K^T, m-tiles of P V
+  uint32_t qb[NC][2];
+  float acc[NC][4];
+  float m[2], l[2];
+  float scale;
+  int cw;
+
+  // the lane's four consecutive int8 channels -> fp16 pairs (bytes 0,1 / 2,3)
+  __device__ static __forceinline__ void i8x4_to_h2(uint32_t r, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = r ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+  }
+  // bytes (0, 2) and (1, 3) of a transposed load -> fp16 pairs
+  __device__ static __forceinline__ void i8x4t_to_h2(uint32_t r, uint32_t& e, uint32_t& o) {
+    const uint32_t u = r ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4240;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4341;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    e = *reinterpret_cast<const uint32_t*>(&ha);
+    o = *reinterpret_cast<const uint32_t*>(&hb);
+  }
+
+  __device__ void init(const __half* qrows, float scale_log2, int cw_, int lane) {
+    cw = cw_;
+    scale = scale_log2;
+    const int n = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        // k = 2t (+8 hf), 2t + 1 (+8 hf) -> channels 16 j + 4 t + 2 hf, + 1
+        uint32_t w = 0;
+        if (n < G) w = *reinterpret_cast<const uint32_t*>(qrows + n * D + 16 * j + 4 * t + 2 * hf);
+        qb[j][hf] = w;
+      }
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // one staged page with nv valid tokens (0 < nv <= S, S a multiple of 16)
+  __device__ void consume(uint8_t* st, int S, int nv, int lane) {
+    const uint32_t kb = smem_u32(st);
+    const uint32_t vb = kb + static_cast<uint32_t>(S) * D;
+    const __half* ksc = reinterpret_cast<const __half*>(st + 2 * S * D);
+    const __half* vsc = ksc + S;
+    if (nv < S) {
+      // V rows past the end: zeros (their p' is 0, but 0 times a stale value
+      // could be NaN inside the product)
+      const int words = (S - nv) * 8;
+      for (int i = lane; i < words; i += 32)
+        *reinterpret_cast<uint4*>(st + S * D + (nv + i / 8) * D + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+    }
+    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    for (int t0 = 0; t0 < nv; t0 += 16) {
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int tok = t0 + (mi & 1) * 8 + r8;
+        const uint32_t rowb = kb + tok * D;
+#pragma unroll
+        for (int j = 0; j < NC; j += 2) {
+          const int chunk = j + (mi >> 1);
+          uint32_t r[4];
+          ldmatrix_x4(r, rowb + ((chunk ^ (tok & 7)) << 4));
+          // r[0]: tokens 0-7 of chunk j, r[1]: tokens 8-15, r[2], r[3]: chunk j + 1
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a[4];
+            i8x4_to_h2(r[2 * h], a[0], a[2]);
+            i8x4_to_h2(r[2 * h + 1], a[1], a[3]);
+            if (h == 0)
+              mma_16816<__half>(c0, a, qb[j][0], qb[j][1]);
+            else
+              mma_16816<__half>(c1, a, qb[j + 1][0], qb[j + 1][1]);
+          }
+        }
+      }
+      const float ks0 = __half2float(ksc[min(t0 + g, S - 1)]);
+      const float ks1 = __half2float(ksc[min(t0 + g + 8, S - 1)]);
+      float sv[4];
+      sv[0] = (c0[0] + c1[0]) * ks0 * scale;
+      sv[1] = (c0[1] + c1[1]) * ks0 * scale;
+      sv[2] = (c0[2] + c1[2]) * ks1 * scale;
+      sv[3] = (c0[3] + c1[3]) * ks1 * scale;
+      const bool v0 = t0 + g < nv, v1 = t0 + g + 8 < nv;
+      if (!v0) sv[0] = sv[1] = -INFINITY;
+      if (!v1) sv[2] = sv[3] = -INFINITY;
+      float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      if (mx0 > m[0]) {
+        const float corr = exp2f(m[0] - mx0);
+        m[0] = mx0;
+        l[0] *= corr;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          acc[j][0] *= corr;
+          acc[j][2] *= corr;
+        }
+      }
+      if (mx1 > m[1]) {
+        const float corr = exp2f(m[1] - mx1);
+        m[1] = mx1;
+        l[1] *= corr;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          acc[j][1] *= corr;
+          acc[j][3] *= corr;
+        }
+      }
+      const float p0 = exp2f(sv[0] - m[0]), p1 = exp2f(sv[1] - m[1]);
+      const float p2 = exp2f(sv[2] - m[0]), p3 = exp2f(sv[3] - m[1]);
+      l[0] += p0 + p2;
+      l[1] += p1 + p3;
+      // p' = 256 p * V scale of the token (0 past the end)
+      const float vs0 = v0 ? 256.f * __half2float(vsc[t0 + g]) : 0.f;
+      const float vs1 = v1 ? 256.f * __half2float(vsc[t0 + g + 8]) : 0.f;
+      const float q0 = p0 * vs0, q1 = p1 * vs0, q2 = p2 * vs1, q3 = p3 * vs1;
+      const uint32_t h01 = pack2<__half>(q0, q1), h23 = pack2<__half>(q2, q3);
+      const float2 f01 = unpack2f<__half>(h01), f23 = unpack2f<__half>(h23);
+      const uint32_t l01 = pack2<__half>(q0 - f01.x, q1 - f01.y);
+      const uint32_t l23 = pack2<__half>(q2 - f23.x, q3 - f23.y);
+      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+      const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+      {
+        // matrices: tokens 0-7 / 8-15 of chunk j (lanes 0-15), then of chunk j + 1
+        const int tok = t0 + ((lane >> 3) & 1) * 8 + r8;
+        const uint32_t rowb = vb + tok * D;
+#pragma unroll
+        for (int j = 0; j < NC; j += 2) {
+          const int chunk = j + (lane >> 4);
+          uint32_t r[4];
+          ldmatrix_x4_trans(r, rowb + ((chunk ^ (tok & 7)) << 4));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a[4];
+            i8x4t_to_h2(r[2 * h], a[0], a[1]);      // tokens 0-7: rows g (ch 2g), g + 8 (ch 2g + 1)
+            i8x4t_to_h2(r[2 * h + 1], a[2], a[3]);  // tokens 8-15
+            mma_16816<__half>(acc[j + h], a, bh0, bh1);
+            mma_16816<__half>(acc[j + h], a, bl0, bl1);
+          }
+        }
+      }
+    }
+  }
+
+  __device__ void fold() {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+    }
+  }
+
+  // rows g / g + 8 of m-tile j hold channels 16 j + 2 g / 16 j + 2 g + 1
+  __device__ void store(float* s_m, float* s_l, float* s_acc, int lane) const {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = 2 * t + e;
+      if (row < G) {
+        if (g == 0) {
+          s_m[cw * G + row] = m[e];
+          s_l[cw * G + row] = l[e];
+        }
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          s_acc[(cw * G + row) * D + 16 * j + 2 * g] = acc[j][e] * (1.f / 256.f);
+          s_acc[(cw * G + row) * D + 16 * j + 2 * g + 1] = acc[j][e + 2] * (1.f / 256.f);
+        }
+      }
+    }
+  }
+};
+
 // Log-sum-exp merge of n states (m, l, acc) for one (row g, channel c):
 // m_i in the log2 domain; returns the merged max, sum and accumulator.
 __device__ __forceinline__ void lse_merge(const float* s_m, const float* s_l, const float* s_acc,

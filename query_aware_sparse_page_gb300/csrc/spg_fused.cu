@@ -31,8 +31,9 @@
 //     consumer); the CTA's partial (m, l, acc) per query row goes into the
 //     leader's shared memory.
 //  4. cluster barrier; the leader merges the partials and writes out / lse.
-// An auxiliary warp of the last CTA applies the Quest append of the new token
-// during the scan (that token's page is forced, so nothing reads its row).
+// An auxiliary warp of the last CTA applies the metadata append of the new
+// token during the scan (Quest min/max of its page; the sketch of a block it
+// completes): that page is forced, so nothing in the step reads it.
 // No CTA waits on another except at the three hardware cluster barriers,
 // which every thread of every CTA reaches on every path; all mbarrier waits
 // are bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still
@@ -67,6 +68,8 @@ struct FusedArgs {
   void* minmax;  // written only by the append
   const uint8_t* sketch;
   const float* sketch_scale;
+  uint8_t* sketch_w;       // the same arrays, written only by the append
+  float* sketch_scale_w;
   const float* proj;
   int32_t* sel;
   int32_t* sel_cnt;
@@ -125,13 +128,116 @@ __device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int 
   }
 }
 
+// Sketch of the block completed by the token at L-1 (when L is a multiple of
+// S; SALS长序列推理优化, the low-rank index key of a block), split over the
+// auxiliary warps of the cluster's C CTAs: CTA r takes tokens
+// [r*S/C, (r+1)*S/C), one token per lane with all DS = 16 sketch dimensions.
+// Keys are dequantised (int8 code times its fp16 scale, exact in fp32) and
+// projected in fp32 with each product rounded and the sum taken in channel
+// order (no fused multiply-add).  Part 1 (during the scan) keeps the lane's
+// values in registers and sends the warp's |max| to every CTA; part 2 (after
+// the scan barrier) forms the block scale absmax / 7 and writes codes
+// rint(v / scale) clamped to [-7, 7], two per byte.  The block is the tail
+// block of this step (forced, never scored), so nothing in the step reads
+// what is written.
+constexpr int kSketchVals = 16;  // one token's 16 sketch values per lane: S / C <= 32
+
+// 16 consecutive channels of a key row as fp32 (row 16-byte aligned)
+template <typename T>
+__device__ __forceinline__ void load16_f32(const T* p, float (&x)[16]) {
+  if constexpr (sizeof(T) == 1) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) x[e] = static_cast<float>(static_cast<int8_t>((ws[e >> 2] >> (8 * (e & 3))) & 0xffu));
+  } else {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) load_cvt<T, 8>(p + 8 * hf, x + 8 * hf);
+  }
+}
+
+template <typename T, int D>
+__device__ void sketch_append_part1(const FusedArgs& a, int b, int h, int L, int lane, uint32_t rank,
+                                    int C, float (&v)[kSketchVals], float* s_samax) {
+  constexpr int DS = 16;
+  const int S = a.S, blk = L / S - 1, tpc = S / C;
+  const int t = static_cast<int>(rank) * tpc + lane;  // this lane's token
+  const int phys = a.page_table[static_cast<size_t>(b) * a.MP + blk];
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < DS; ++u) v[u] = 0.f;
+  if (phys >= 0 && phys < a.n_phys) {
+    if (lane < tpc) {
+      const size_t ph = static_cast<size_t>(phys) * a.Hkv + h;
+      const T* krow = static_cast<const T*>(a.k_pool) + (ph * S + t) * D;
+      float sc = 1.f;
+      if constexpr (is_i8<T>()) sc = __half2float(a.k_scale[ph * S + t]);
+      const float4* P4 = reinterpret_cast<const float4*>(a.proj);  // [D][DS] row-major
+      for (int ic = 0; ic < D; ic += 16) {
+        float x[16];
+        load16_f32<T>(krow + ic, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float kv = x[e];
+          if constexpr (is_i8<T>()) kv = __fmul_rn(kv, sc);
+#pragma unroll
+          for (int q4 = 0; q4 < DS / 4; ++q4) {
+            const float4 pv = __ldg(P4 + (ic + e) * (DS / 4) + q4);
+            v[4 * q4] = __fadd_rn(v[4 * q4], __fmul_rn(kv, pv.x));
+            v[4 * q4 + 1] = __fadd_rn(v[4 * q4 + 1], __fmul_rn(kv, pv.y));
+            v[4 * q4 + 2] = __fadd_rn(v[4 * q4 + 2], __fmul_rn(kv, pv.z));
+            v[4 * q4 + 3] = __fadd_rn(v[4 * q4 + 3], __fmul_rn(kv, pv.w));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < DS; ++u) amax = fmaxf(amax, fabsf(v[u]));
+    }
+  } else if (lane == 0 && rank == 0) {
+    record_error(a.err, SPG_DEVERR_PAGE_ID);
+  }
+  amax = warp_max(amax);
+  // every CTA's aux warp needs every CTA's |max| after the scan barrier
+  if (lane < C) st_cluster_f32(map_rank(s_samax + rank, static_cast<uint32_t>(lane)), amax);
+}
+
+template <typename T, int D>
+__device__ void sketch_append_part2(const FusedArgs& a, int b, int h, int L, int lane, uint32_t rank,
+                                    int C, const float (&v)[kSketchVals], const float* s_samax) {
+  constexpr int DS = 16;
+  const int S = a.S, blk = L / S - 1, tpc = S / C;
+  const int t = static_cast<int>(rank) * tpc + lane;
+  const int phys = a.page_table[static_cast<size_t>(b) * a.MP + blk];
+  if (phys < 0 || phys >= a.n_phys) return;
+  float amax = 0.f;
+  for (int r = 0; r < C; ++r) amax = fmaxf(amax, s_samax[r]);
+  const float scale = amax > 0.f ? __fdiv_rn(amax, 7.0f) : 1.0f;
+  const size_t lrow = (static_cast<size_t>(b) * a.Hkv + h) * a.MP + blk;
+  if (lane < tpc) {
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < DS / 2; ++k) {
+      const int c0 = max(-7, min(7, static_cast<int>(rintf(__fdiv_rn(v[2 * k], scale)))));
+      const int c1 = max(-7, min(7, static_cast<int>(rintf(__fdiv_rn(v[2 * k + 1], scale)))));
+      w[k >> 2] |= static_cast<uint32_t>((c0 & 0xf) | ((c1 & 0xf) << 4)) << (8 * (k & 3));
+    }
+    *reinterpret_cast<uint2*>(a.sketch_w + (lrow * S + t) * (DS / 2)) = make_uint2(w[0], w[1]);
+  }
+  if (rank == 0 && lane == 0) a.sketch_scale_w[lrow] = scale;
+}
+
 template <typename T, typename TQ, int D, int G, int SEL>
 __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     k_fused(const __grid_constant__ FusedArgs a) {
   constexpr int CW = kConsumerWarps;
-  constexpr bool MMA = !is_i8<T>();  // tensor-core consumer, TMA tile producer
+  // consumer: 1 = tensor cores on fp16/bf16 pages, 2 = tensor cores on int8
+  // pages (D = 128, fp16 query), 0 = CUDA cores; 1 and 2 take TMA tiles
+  constexpr int CONS = !is_i8<T>() ? 1 : ((D == 128 && std::is_same<TQ, __half>::value) ? 2 : 0);
+  constexpr bool MMA = CONS != 0;
   const int C = a.cluster;
-  using Consumer = std::conditional_t<MMA, AttnMma<T, D, G>, AttnConsumer<T, D, G, 1>>;
+  using Consumer = std::conditional_t<
+      CONS == 1, AttnMma<T, D, G>,
+      std::conditional_t<CONS == 2, AttnMmaI8<G>, AttnConsumer<T, D, G, 1>>>;
 
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // TMA tiles with 128-byte swizzle want 1024-byte aligned destinations
@@ -141,6 +247,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   __shared__ int s_qc[4];
   __shared__ float s_sq;
   __shared__ int s_natt;  // pages of the selection this CTA attends to
+  __shared__ float s_samax[kMaxCluster];  // sketch append: each CTA's |max|
+  float sk_v[SEL ? kSketchVals : 1];       // sketch append: this lane's projected values
 
   const int S = a.S, STAGES = a.stages, R = a.rows_per_stage, PPS = a.pages_per_stage;
   const uint32_t sbytes = a.stage_bytes, rb = a.row_bytes, pbytes = a.page_bytes;
@@ -232,11 +340,17 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       if (lane == 0) mbar_arrive(&full[stage]);
     }
   } else if (warp == CW + 1) {
-    // auxiliary warp: the Quest append of the token at L-1.  Its page is
+    // auxiliary warp: the metadata append of the token at L-1.  Its page is
     // forced (n_recent >= 1), so neither this step's scan nor its attend
-    // reads that metadata row; done here it overlaps the scan.
-    if constexpr (SEL == 0)
+    // reads that metadata; done here it overlaps the scan.
+    if constexpr (SEL == 0) {
       if (a.append && rank == C - 1 && L > 0) append_minmax_warp<T, D>(a, b, h, L, lane);
+    } else {
+      // the sketch of a block is written when the block fills (every CTA's
+      // aux warp takes a slice)
+      if (a.append && L > 0 && L % S == 0)
+        sketch_append_part1<T, D>(a, b, h, L, lane, rank, C, sk_v, s_samax);
+    }
   } else {
     // consumers
     uint32_t kmn = 0xffffffffu, kmx = 0u;  // of the keys this warp produces
@@ -318,20 +432,23 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
         }
         const int nr = min(R, rows - ks * R);
         const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
-        for (int r = 0; r < nr; ++r) {  // the stage's blocks
-          uint2 wk[4];
+        for (int r0 = 0; r0 < nr; r0 += 4) {  // the stage's blocks, four at a time
+          const int nb = min(4, nr - r0);
+          float cz[4], score[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (lane + 32 * k < S)
-              wk[k] = *reinterpret_cast<const uint2*>(st + r * rb + (lane + 32 * k) * 8);
-          const float cz =
-              __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r]), a.inv_sqrt_d);
-          const float score = sketch_block_score(wk, S, qc, cz);
+          for (int r = 0; r < 4; ++r)
+            cz[r] = r < nb ? __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r0 + r]), a.inv_sqrt_d)
+                           : 0.f;
+          sketch_block_scores4(st + r0 * rb, rb, nb, S, qc, cz, score);
           if (lane == 0) {
-            const uint32_t k0 = score_key(score);
-            st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r - lo), k0);
-            kmn = min(kmn, k0);
-            kmx = max(kmx, k0);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              if (r < nb) {
+                const uint32_t k0 = score_key(score[r]);
+                st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r0 + r - lo), k0);
+                kmn = min(kmn, k0);
+                kmx = max(kmx, k0);
+              }
           }
         }
         __syncwarp();
@@ -346,6 +463,11 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     }
   }
   cluster_sync();  // every key (and every warp's key min / max) is in the leader
+
+  if constexpr (SEL == 1) {
+    if (warp == CW + 1 && a.append && L > 0 && L % S == 0)
+      sketch_append_part2<T, D>(a, b, h, L, lane, rank, C, sk_v, s_samax);
+  }
 
   // ------------------------------------------------------------- selection
   if (rank == 0) {
@@ -441,12 +563,17 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
             const size_t row = static_cast<size_t>(ph) * Hkv + h;
             mbar_expect_tx(&full[stage], 2 * tile + 2 * scb);
             if constexpr (MMA) {
-              // D / 64 swizzled tiles of [S][64] for K, then for V
+              // swizzled tiles of [S rows][128 bytes] for K, then for V
+              constexpr int NT = D * static_cast<int>(sizeof(T)) / 128, EPT = 128 / sizeof(T);
               const int y = static_cast<int>(row) * S;
 #pragma unroll
-              for (int hf = 0; hf < D / 64; ++hf) {
-                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * 64, y, &full[stage], pol);
-                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * 64, y, &full[stage], pol);
+              for (int hf = 0; hf < NT; ++hf) {
+                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
+                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
+              }
+              if constexpr (is_i8<T>()) {
+                bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
+                bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
               }
             } else {
               bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
@@ -541,7 +668,9 @@ template <typename T, typename TQ, int D, int G>
 cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   constexpr int threads = (kConsumerWarps + 2) * 32;  // + producer + auxiliary warp
   const int S = p.page_size;
-  const uint32_t pb = kv_stage_bytes<T, D>(S);
+  constexpr bool MMA = !is_i8<T>() || (D == 128 && std::is_same<TQ, __half>::value);
+  // a page's K tile must start 1024-byte aligned for the swizzled TMA tiles
+  const uint32_t pb = MMA ? (kv_stage_bytes<T, D>(S) + 1023u) & ~1023u : kv_stage_bytes<T, D>(S);
   const uint32_t rb = p.selector == SPG_SEL_QUEST ? 2u * D * sizeof(T) : static_cast<uint32_t>(S) * 8u;
   int pps = 1;
   while (pps * 2 <= kMaxPagesPerStage && (pps * 2) * pb <= static_cast<uint32_t>(kStageBytesTarget))
@@ -570,7 +699,7 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
                            sizeof(int) * 2 * n_sel_pages(p);
   const size_t smem = 1024 + att_off + att_bytes;  // + alignment slack
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
-  if constexpr (!is_i8<T>()) {
+  if constexpr (MMA) {
     const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
     if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S) ||
         !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S))
@@ -603,6 +732,15 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   int C = kMaxCluster;
   while (C > 2 && units * C > slots) C /= 2;
   a.cluster = C;
+  // sketch scan stages sized so that each consumer warp gets about one
+  // stage of the CTA's chunk of blocks (the stage buffers stay as planned)
+  if (p.selector == SPG_SEL_SKETCH_INT4) {
+    const int cpc_max = (p.max_pages_per_seq + C - 1) / C;
+    a.rows_per_stage = std::min(R, std::max(4, (cpc_max + kConsumerWarps - 1) / kConsumerWarps));
+  }
+  // the sketch append gives each aux-warp lane one token of the block
+  if (a.append && p.selector == SPG_SEL_SKETCH_INT4 && S > C * 32)
+    return cudaErrorNotSupported;  // the caller falls back to the separate append
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(C, units);
   cfg.blockDim = dim3(threads);
@@ -643,7 +781,8 @@ bool fused_supported(const spg_params& p, int append) {
   if (p.selector != SPG_SEL_QUEST && p.selector != SPG_SEL_SKETCH_INT4) return false;
   if (p.max_pages_per_seq > kFusedMaxPages) return false;
   if (p.selector == SPG_SEL_SKETCH_INT4 && p.page_size > 128) return false;
-  if (append && (p.selector != SPG_SEL_QUEST || p.n_recent_pages < 1)) return false;
+  if (append && p.n_recent_pages < 1) return false;  // the appended token's page must be forced
+  if (append && p.selector == SPG_SEL_SKETCH_INT4 && p.sketch_dim != 16) return false;
   return true;
 }
 
@@ -664,6 +803,9 @@ cudaError_t launch_fused(const spg_params& p, const void* q, const void* k_pool,
   a.minmax = minmax;
   a.sketch = sketch;
   a.sketch_scale = sketch_scale;
+  // with append, the caller (sparse_decode_step) owns writable sketch arrays
+  a.sketch_w = append ? const_cast<uint8_t*>(sketch) : nullptr;
+  a.sketch_scale_w = append ? const_cast<float*>(sketch_scale) : nullptr;
   a.proj = proj;
   a.sel = sel;
   a.sel_cnt = sel_cnt;

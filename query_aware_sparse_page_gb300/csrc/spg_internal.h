@@ -25,8 +25,8 @@ size_t workspace_bytes(const spg_params& p);
 
 // Tensor map of a K or V pool viewed as a 2-D array [rows][head_dim]
 // (rows = num_phys_pages * num_kv_heads * page_size) whose tile is one page
-// of one kv-head, 64 channels wide (128 bytes, 128-byte swizzle): a page is
-// copied as head_dim / 64 tiles.  False when the pool cannot be described
+// of one kv-head, 128 bytes wide (64 fp16/bf16 channels or 128 int8 ones,
+// 128-byte swizzle): a page is copied as head_dim * elem_bytes / 128 tiles.  False when the pool cannot be described
 // (dtype, alignment, size) or the encoder is unavailable.
 bool make_kv_tmap(CUtensorMap* map, const void* pool, int kv_dtype, long long rows, int head_dim,
                   int page_size);

@@ -655,4 +655,54 @@ __device__ __forceinline__ float sketch_block_score(const uint2 (&wk)[4], int S,
   return zmax + logf(sum);
 }
 
+// Scores of nb <= 4 consecutive sketch blocks of a staged tile (block r at
+// tile + r * rb: S tokens x 8 bytes of int4 codes) by one warp, with the
+// four blocks' reductions interleaved: z = dot(codes, qc) * cz[r], score =
+// max z + ln sum exp(z - max z) over the block's S <= 128 tokens.
+__device__ __forceinline__ void sketch_block_scores4(const uint8_t* tile, int rb, int nb, int S,
+                                                     const int* qc, const float (&cz)[4],
+                                                     float (&score)[4]) {
+  const int lane = threadIdx.x & 31;
+  constexpr float kL2e = 1.4426950408889634f;
+  float z[4][4], zmax[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    zmax[r] = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      z[r][k] = -INFINITY;
+      if (r < nb && lane + 32 * k < S) {
+        const uint2 w = *reinterpret_cast<const uint2*>(tile + r * rb + (lane + 32 * k) * 8);
+        int e0, o0, e1, o1;
+        unpack_int4x8(w.x, e0, o0);
+        unpack_int4x8(w.y, e1, o1);
+        int dot = __dp4a(e0, qc[0], 0);
+        dot = __dp4a(o0, qc[1], dot);
+        dot = __dp4a(e1, qc[2], dot);
+        dot = __dp4a(o1, qc[3], dot);
+        z[r][k] = static_cast<float>(dot) * cz[r] * kL2e;  // log2 domain
+        zmax[r] = fmaxf(zmax[r], z[r][k]);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) zmax[r] = fmaxf(zmax[r], __shfl_xor_sync(0xffffffffu, zmax[r], o));
+  float sum[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    sum[r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (r < nb && lane + 32 * k < S) sum[r] += exp2f(z[r][k] - zmax[r]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) score[r] = (zmax[r] + log2f(sum[r])) * kLn2;
+}
+
 }  // namespace spg

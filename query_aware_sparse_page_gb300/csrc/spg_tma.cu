@@ -29,18 +29,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool make_kv_tmap(CUtensorMap* map, const void* pool, int kv_dtype, long long rows, int head_dim,
                   int page_size) {
-  if (kv_dtype != SPG_F16 && kv_dtype != SPG_BF16) return false;
-  if (head_dim % 64 != 0 || page_size < 8 || page_size > 256) return false;
+  const int esz = kv_dtype == SPG_I8 ? 1 : 2;
+  if (kv_dtype != SPG_F16 && kv_dtype != SPG_BF16 && kv_dtype != SPG_I8) return false;
+  if ((head_dim * esz) % 128 != 0 || page_size < 8 || page_size > 256) return false;
   if (rows < 1 || rows > 0x7fffffffLL) return false;  // int32 row coordinates
   if ((reinterpret_cast<uintptr_t>(pool) & 15u) != 0) return false;
   const auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2u};
-  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(page_size)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * esz};
+  const cuuint32_t box[2] = {128u / esz, static_cast<cuuint32_t>(page_size)};  // 128-byte rows
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r =
-      fn(map, kv_dtype == SPG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+      fn(map,
+         kv_dtype == SPG_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+         : kv_dtype == SPG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : CU_TENSOR_MAP_DATA_TYPE_UINT8,
          2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
