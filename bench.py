@@ -41,8 +41,9 @@ NOMINAL_HBM_GBS = 8000.0
 # that workload, and the sha256 of the kernel sources it was taken on
 # (profiles/k_fused_<workload>.md).  Reported only while the sources match.
 NCU_TRAFFIC = {
-    "llama2-7b-mha-32k": (67_919_360, "ca081df70fc8e95b575012a49c8438d4460d57e4d640849292c8fc1e62fe00e5"),
-    "long-scan-b4-128k": (205_535_232, "ca081df70fc8e95b575012a49c8438d4460d57e4d640849292c8fc1e62fe00e5"),
+    "llama2-7b-mha-32k": (67_831_552, "636eaf1c57d051e68f8835d2d18c1f7d0936b3176a9270b9276bdb69549d217b"),
+    "long-scan-b4-128k": (205_298_688, "636eaf1c57d051e68f8835d2d18c1f7d0936b3176a9270b9276bdb69549d217b"),
+    "sals-int8-b16-10k-4x": (100_465_408, "636eaf1c57d051e68f8835d2d18c1f7d0936b3176a9270b9276bdb69549d217b"),
 }
 
 
