@@ -11,24 +11,19 @@
 // contiguous range of the unit's page list (selected ids, or every page for
 // the dense baseline) and is warp-specialised:
 //  * the producer warp resolves logical -> physical page ids 32 at a time
-//    (one lane per page), then lane 0 streams each page's contiguous K and V
-//    tiles ([S][d] of one kv-head in the [P][Hkv][S][d] pools, plus the
-//    per-token fp16 scales for int8) into a STAGES-deep shared-memory ring
-//    with cp.async.bulk (the TMA bulk-copy engine), one "full" mbarrier per
-//    stage carrying the byte count;
-//  * four consumer warps share every stage: each takes 4 tokens of each
-//    16-token round (8 lanes per token; 2 tokens and 16 lanes per token when
-//    the group has 4 or 8 query rows, to bound registers), computes the G
-//    query rows' logits on CUDA cores with a 3- or 4-step shuffle reduction,
-//    keeps a warp-wide running max per row and a per-lane accumulator for
-//    its token's channels, and releases the stage on an "empty" mbarrier
-//    (4 arrivals).
-// A lane's channels are 16-byte chunks lt, lt + LPT, ... of the row (or one
-// smaller piece), so the lanes of a token hit distinct bank groups and every
-// shared load runs at the minimum number of wavefronts.  Each of the G query
-// rows of the kv-head group reuses every staged tile (GQA).  All waits are
-// bounded; a wait that runs out records SPG_DEVERR_TIMEOUT and the CTA drains
-// (again bounded) the copies it issued before it leaves.
+//    (one lane per page) and streams each page's K and V tiles ([S][d] of one
+//    kv-head in the [P][Hkv][S][d] pools, plus the per-token fp16 scales for
+//    int8) into a shared-memory ring of stages of up to 8 pages, one lane per
+//    page: 2-D TMA tiles with 128-byte swizzle for the tensor-core consumers,
+//    cp.async.bulk otherwise; one "full" mbarrier per stage carries the bytes;
+//  * stage k belongs to consumer warp k % 4, which runs the flash-decoding
+//    consumer over its pages (tensor cores for fp16/bf16 pages and for int8
+//    pages of head_dim 128 with an fp16 query, CUDA cores otherwise) and
+//    releases the stage on its "empty" mbarrier.
+// Each of the G query rows of the kv-head group reuses every staged tile
+// (GQA).  All waits are bounded; a wait that runs out records
+// SPG_DEVERR_TIMEOUT and the CTA drains (again bounded) the copies it issued
+// before it leaves.
 //
 // Partials per (batch, q-head, split): running max m (log2 domain, scale
 // folded in), running sum l, unnormalised accumulator acc[d].  The last CTA
@@ -43,9 +38,12 @@
 namespace spg {
 namespace {
 
-constexpr int kRingBytesTarget = 56 * 1024;
+constexpr int kRingBytesTarget = 64 * 1024;
+constexpr int kStageBytesTarget = 16 * 1024;
+constexpr int kMaxPagesPerStage = 8;
 
 struct AttnArgs {
+  CUtensorMap tmk, tmv;  // K / V pools as page tiles (tensor-core consumers)
   const void* q;
   const void* k_pool;
   const void* v_pool;
@@ -62,24 +60,35 @@ struct AttnArgs {
   float* out;
   float* lse;
   int32_t* err;
-  int Hkv, S, MP, n_phys, n_sel, pages_per_split, stages;
+  int Hkv, S, MP, n_phys, n_sel, pages_per_split, stages, pages_per_stage;
+  uint32_t stage_bytes, page_bytes;
   float scale_log2;
 };
 
 template <typename T, typename TQ, int D, int G>
-__global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_attn(const AttnArgs a) {
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
+    k_attn(const __grid_constant__ AttnArgs a) {
   constexpr int CW = kConsumerWarps;
-  using Consumer = AttnConsumer<T, D, G>;
+  // consumer: 1 = tensor cores on fp16/bf16 pages, 2 = tensor cores on int8
+  // pages (D = 128, fp16 query), 0 = CUDA cores; 1 and 2 take TMA tiles
+  constexpr int CONS = !is_i8<T>() ? 1 : ((D == 128 && std::is_same<TQ, __half>::value) ? 2 : 0);
+  constexpr bool MMA = CONS != 0;
+  using Consumer = std::conditional_t<
+      CONS == 1, AttnMma<T, D, G>,
+      std::conditional_t<CONS == 2, AttnMmaI8<G>, AttnConsumer<T, D, G, 1>>>;
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // TMA tiles with 128-byte swizzle want 1024-byte aligned destinations
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = a.S;
-  const int STAGES = a.stages;
+  const int STAGES = a.stages, PPS = a.pages_per_stage;
   const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
   const uint32_t scb = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
-  const uint32_t sbytes = kv_stage_bytes<T, D>(S);
+  const uint32_t sbytes = a.stage_bytes, pbytes = a.page_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(STAGES) * sbytes);
   uint64_t* empty = full + kMaxStages;
-  int* s_nv = reinterpret_cast<int*>(empty + kMaxStages);
+  int* s_np = reinterpret_cast<int*>(empty + kMaxStages);  // [stages] pages in stage
+  int* s_nv = s_np + kMaxStages;                          // [stages][8] valid tokens
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,9 +100,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_attn(const AttnAr
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CW);
+      mbar_init(&empty[s], 1);
     }
     mbar_fence_init();
+  }
+  if constexpr (MMA) {
+    if (threadIdx.x == CW * 32) {
+      tma_prefetch_desc(&a.tmk);
+      tma_prefetch_desc(&a.tmv);
+    }
   }
   pdl_wait();  // sel / sel_cnt (and anything else) may come from the previous kernel
 
@@ -113,16 +128,16 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_attn(const AttnAr
   }
   const int s0 = split * a.pages_per_split;
   const int n_range = max(min(s0 + a.pages_per_split, count) - s0, 0);
+  const int n_st = (n_range + PPS - 1) / PPS;
   __syncthreads();
 
   Consumer cons;
 
   if (warp == CW) {
-    // ---------------- producer: page ids, then bulk copies into the ring
+    // ---------------- producer: page ids, then one lane per page of a stage
     const T* kpool = static_cast<const T*>(a.k_pool);
     const T* vpool = static_cast<const T*>(a.v_pool);
     const uint64_t pol = policy_evict_first();
-    int issued = 0;
     bool ok = true;
     for (int base = 0; base < n_range && ok; base += 32) {
       int ph = -1, nv = 0;
@@ -143,56 +158,73 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32) k_attn(const AttnAr
         }
       }
       const int nb = min(32, n_range - base);
-      for (int jj = 0; jj < nb; ++jj) {
-        const int phj = __shfl_sync(0xffffffffu, ph, jj);
-        const int nvj = __shfl_sync(0xffffffffu, nv, jj);
-        const int k = base + jj;
-        const int stage = k % STAGES;
-        if (lane == 0) {
-          if (k >= STAGES && !mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1)) {
-            record_error(a.err, SPG_DEVERR_TIMEOUT);
-            ok = false;
-          }
-          if (ok) {
-            uint8_t* dst = smem + static_cast<size_t>(stage) * sbytes;
-            s_nv[stage] = phj >= 0 ? nvj : 0;
-            if (phj < 0) {
-              mbar_arrive_expect_tx(&full[stage], 0);
+      for (int t0 = 0; t0 < nb && ok; t0 += PPS) {
+        const int k = (base + t0) / PPS, stage = k % STAGES;
+        bool lok = true;
+        if (lane == 0 && k >= STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
+        if (!lok) record_error(a.err, SPG_DEVERR_TIMEOUT);
+        ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const int np = min(PPS, nb - t0);
+        if (lane >= t0 && lane < t0 + np) {
+          const int i = lane - t0;
+          uint8_t* dst = smem + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes;
+          s_nv[stage * kMaxPagesPerStage + i] = ph >= 0 ? nv : 0;
+          if (ph >= 0) {
+            const size_t row = static_cast<size_t>(ph) * Hkv + h;
+            mbar_expect_tx(&full[stage], 2 * tile + 2 * scb);
+            if constexpr (MMA) {
+              // swizzled tiles of [S rows][128 bytes] for K, then for V
+              constexpr int NT = D * static_cast<int>(sizeof(T)) / 128, EPT = 128 / sizeof(T);
+              const int y = static_cast<int>(row) * S;
+#pragma unroll
+              for (int hf = 0; hf < NT; ++hf) {
+                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
+                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
+              }
             } else {
-              const size_t row = static_cast<size_t>(phj) * Hkv + h;
-              mbar_arrive_expect_tx(&full[stage], sbytes);
               bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
               bulk_g2s_hint(dst + tile, vpool + row * S * D, tile, &full[stage], pol);
-              if constexpr (is_i8<T>()) {
-                bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
-                bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
-              }
             }
-            ++issued;
+            if constexpr (is_i8<T>()) {
+              bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
+              bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
+            }
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        if (lane == 0) s_np[stage] = np;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
       }
     }
-    issued = __shfl_sync(0xffffffffu, issued, 0);
     if (!ok && lane == 0) {
-      // drain the copies still in flight before the CTA can leave
-      for (int k = max(0, issued - STAGES); k < issued; ++k)
+      // drain the copies still in flight before the CTA can leave (bounded
+      // waits; uses that were never issued simply time out)
+      for (int k = max(0, n_st - STAGES); k < n_st; ++k)
         mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
     }
   } else {
-    // ---------------- consumers
+    // ---------------- consumers: stage k belongs to warp k % CW
     cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
               a.scale_log2, warp, lane);
-    for (int k = 0; k < n_range; ++k) {
+    for (int k = warp; k < n_st; k += CW) {
       const int stage = k % STAGES;
       if (!mbar_wait_bounded(&full[stage], (k / STAGES) & 1)) {
         if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
         break;
       }
-      const int nv = s_nv[stage];
-      if (nv > 0) cons.consume(smem + static_cast<size_t>(stage) * sbytes, S, nv);
+      const int np = s_np[stage];
+      for (int i = 0; i < np; ++i) {
+        const int nv = s_nv[stage * kMaxPagesPerStage + i];
+        uint8_t* pg = smem + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes;
+        if (nv > 0) {
+          if constexpr (MMA)
+            cons.consume(pg, S, nv, lane);
+          else
+            cons.consume(pg, S, nv);
+        }
+      }
+      if constexpr (MMA) fence_proxy_async();  // zeroed slots before the next TMA write
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
@@ -280,36 +312,51 @@ template <typename T, typename TQ, int D, int G>
 cudaError_t attn_typed(const spg_params& p, const AttnArgs& a0, int pages_upper, float* out,
                        float* lse, cudaStream_t st) {
   constexpr int threads = (kConsumerWarps + 1) * 32;
+  constexpr bool MMA = !is_i8<T>() || (D == 128 && std::is_same<TQ, __half>::value);
   AttnArgs a = a0;
+  const int S = p.page_size;
   const int units = p.batch * p.num_kv_heads;
-  const uint32_t sb = kv_stage_bytes<T, D>(p.page_size);
-  const int stages = max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb)));
+  // a page's K tile must start 1024-byte aligned for the swizzled TMA tiles
+  const uint32_t pb = MMA ? (kv_stage_bytes<T, D>(S) + 1023u) & ~1023u : kv_stage_bytes<T, D>(S);
+  int pps = 1;
+  while (pps * 2 <= kMaxPagesPerStage && (pps * 2) * pb <= static_cast<uint32_t>(kStageBytesTarget))
+    pps *= 2;
+  const uint32_t sb = pps * pb;
+  // a multiple of the consumer warps: each ring slot has one owner
+  int stages = max(2, min(kMaxStages, static_cast<int>(kRingBytesTarget / sb)));
+  stages = (stages + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+  if (stages > kMaxStages) return cudaErrorNotSupported;
   a.stages = stages;
+  a.pages_per_stage = pps;
+  a.stage_bytes = sb;
+  a.page_bytes = pb;
+  if constexpr (MMA) {
+    const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
+    if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S) ||
+        !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S))
+      return cudaErrorNotSupported;
+  }
   auto kern = k_attn<T, TQ, D, G>;
   const size_t ring = static_cast<size_t>(stages) * sb;
-  const size_t bars = sizeof(uint64_t) * 2 * kMaxStages + sizeof(int) * kMaxStages;
+  const size_t bars = sizeof(uint64_t) * 2 * kMaxStages +
+                      sizeof(int) * (kMaxStages + kMaxStages * kMaxPagesPerStage);
   const size_t merge = sizeof(float) * kConsumerWarps * G * (D + 2);
   const size_t comb = sizeof(float) * (G * kMaxSplits + 2 * G);
-  const size_t smem = max(ring + bars, max(merge, comb));
+  const size_t smem = 1024 + max(ring + bars, max(merge, comb));  // + alignment slack
+  if (smem > 227u * 1024u) return cudaErrorNotSupported;
   cudaError_t e = ensure_smem(kern, smem);
   if (e != cudaSuccess) return e;
   // one wave: as many CTAs as fit on the GPU at once, spread over the units
-  static int per_sm_cache[2] = {0, 0};  // (smem bytes, CTAs per SM) of the last query
-  int per_sm = per_sm_cache[0] == static_cast<int>(smem) ? per_sm_cache[1] : 0;
-  if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) !=
-            cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    per_sm_cache[0] = static_cast<int>(smem);
-    per_sm_cache[1] = per_sm;
-  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
   const int slots = device_sm_count() * per_sm;
   int n_split = max(1, slots / units);
   n_split = min(n_split, min(kMaxSplits, max(pages_upper, 1)));
-  const int pps = (max(pages_upper, 1) + n_split - 1) / n_split;
-  n_split = max(1, (max(pages_upper, 1) + pps - 1) / pps);
-  a.pages_per_split = pps;
+  const int pps_split = (max(pages_upper, 1) + n_split - 1) / n_split;
+  n_split = max(1, (max(pages_upper, 1) + pps_split - 1) / pps_split);
+  a.pages_per_split = pps_split;
   a.out = out;
   a.lse = lse;
   return launch_pdl(kern, dim3(n_split, units), dim3(threads), smem, st, a);
