@@ -44,6 +44,7 @@ constexpr int kMaxPagesPerStage = 8;
 
 struct AttnArgs {
   CUtensorMap tmk, tmv;  // K / V pools as page tiles (tensor-core consumers)
+  int whole_page;        // the maps are 3-D: one copy per page
   const void* q;
   const void* k_pool;
   const void* v_pool;
@@ -177,10 +178,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
               // swizzled tiles of [S rows][128 bytes] for K, then for V
               constexpr int NT = D * static_cast<int>(sizeof(T)) / 128, EPT = 128 / sizeof(T);
               const int y = static_cast<int>(row) * S;
+              if (a.whole_page) {
+                tma_load_3d(dst, &a.tmk, 0, y, 0, &full[stage], pol);
+                tma_load_3d(dst + tile, &a.tmv, 0, y, 0, &full[stage], pol);
+              } else {
 #pragma unroll
-              for (int hf = 0; hf < NT; ++hf) {
-                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
-                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
+                for (int hf = 0; hf < NT; ++hf) {
+                  tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
+                  tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
+                }
               }
             } else {
               bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
@@ -332,9 +338,11 @@ cudaError_t attn_typed(const spg_params& p, const AttnArgs& a0, int pages_upper,
   a.page_bytes = pb;
   if constexpr (MMA) {
     const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
-    if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S) ||
-        !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S))
+    bool wk = false, wv = false;
+    if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S, &wk) ||
+        !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S, &wv) || wk != wv)
       return cudaErrorNotSupported;
+    a.whole_page = wk ? 1 : 0;
   }
   auto kern = k_attn<T, TQ, D, G>;
   const size_t ring = static_cast<size_t>(stages) * sb;

@@ -58,6 +58,7 @@ constexpr int kRingBytesTarget = 64 * 1024;
 
 struct FusedArgs {
   CUtensorMap tmk, tmv;  // K / V pools as page tiles (fp16/bf16 pools)
+  int whole_page;        // the maps are 3-D: one copy per page
   const void* q;
   const void* k_pool;
   const void* v_pool;
@@ -566,10 +567,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
               // swizzled tiles of [S rows][128 bytes] for K, then for V
               constexpr int NT = D * static_cast<int>(sizeof(T)) / 128, EPT = 128 / sizeof(T);
               const int y = static_cast<int>(row) * S;
+              if (a.whole_page) {
+                tma_load_3d(dst, &a.tmk, 0, y, 0, &full[stage], pol);
+                tma_load_3d(dst + tile, &a.tmv, 0, y, 0, &full[stage], pol);
+              } else {
 #pragma unroll
-              for (int hf = 0; hf < NT; ++hf) {
-                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
-                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
+                for (int hf = 0; hf < NT; ++hf) {
+                  tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
+                  tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
+                }
               }
               if constexpr (is_i8<T>()) {
                 bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
@@ -701,9 +707,11 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
   if constexpr (MMA) {
     const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
-    if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S) ||
-        !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S))
+    bool wk = false, wv = false;
+    if (!make_kv_tmap(&a.tmk, a.k_pool, p.kv_dtype, rows, D, S, &wk) ||
+        !make_kv_tmap(&a.tmv, a.v_pool, p.kv_dtype, rows, D, S, &wv) || wk != wv)
       return cudaErrorNotSupported;
+    a.whole_page = wk ? 1 : 0;
   }
   a.stages = stages;
   a.rows_per_stage = R;

@@ -23,13 +23,16 @@ struct Workspace {
 
 size_t workspace_bytes(const spg_params& p);
 
-// Tensor map of a K or V pool viewed as a 2-D array [rows][head_dim]
-// (rows = num_phys_pages * num_kv_heads * page_size) whose tile is one page
-// of one kv-head, 128 bytes wide (64 fp16/bf16 channels or 128 int8 ones,
-// 128-byte swizzle): a page is copied as head_dim * elem_bytes / 128 tiles.  False when the pool cannot be described
-// (dtype, alignment, size) or the encoder is unavailable.
+// Tensor map of a K or V pool (rows = num_phys_pages * num_kv_heads *
+// page_size rows of head_dim elements) through which one page of one kv-head
+// lands in shared memory as head_dim * elem_bytes / 128 tiles of [page_size
+// rows][128 bytes] (64 fp16/bf16 channels or 128 int8 ones each, 128-byte
+// swizzle).  *whole_page: the map is 3-D and one copy (coordinates {0, row,
+// 0}) brings the whole page; else it is 2-D and each tile is one copy
+// (coordinates {64-channel slice start, row}).  False when the pool cannot be
+// described (dtype, alignment, size) or the encoder is unavailable.
 bool make_kv_tmap(CUtensorMap* map, const void* pool, int kv_dtype, long long rows, int head_dim,
-                  int page_size);
+                  int page_size, bool* whole_page);
 Workspace carve_workspace(const spg_params& p, void* ws);
 
 int n_sel_pages(const spg_params& p);

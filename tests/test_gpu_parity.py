@@ -11,12 +11,12 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import decode, quest, sketch as osk
+from oracle import decode, quest, select as oselect, sketch as osk
 from synth import get_workload, make_inputs, scaled
 
 from conftest import oracle_inputs, oracle_params, to_numpy
 from gpu_helpers import (TOL_OUT, assert_paths_agree, check_unit, gpu_selection, run_step,
-                         unswizzle_meta_row)
+                         unit_inputs, unswizzle_meta_row)
 
 pytestmark = pytest.mark.gpu
 
@@ -262,6 +262,67 @@ def test_all_equal_scores_take_lowest_pages():
     inp.k_pool[:] = inp.k_pool[0:1, :, :, :]  # every page the same
     _, bufs, _ = run_step(inp)
     assert gpu_selection(bufs, 0, 0) == [0, 1, 2, 3, 4, 5, 39]
+
+
+def _integer_score_inputs(kind, n_pages=1200, n_sel=100):
+    """Pages whose tokens all equal v * e_0 (v an integer, exact in fp16) and
+    queries e_0: the Quest bound of a page is exactly v in fp32 and in fp64,
+    so ties are exact and the selection has one right answer, also inside
+    the tie band.  1200 pages spread each unit's candidates over a cluster
+    of 8 CTAs."""
+    w = scaled(get_workload("llama2-7b-mha-32k"), num_q_heads=4, num_kv_heads=4,
+               seq_len=16 * n_pages + 5, n_sel_pages=n_sel, needles_per_head=0)
+    inp = make_inputs(w, device=DEV)
+    g = torch.Generator().manual_seed(11)
+    shape = (inp.k_pool.shape[0], w.num_kv_heads)
+    if kind == "three-values":  # ~400 pages tie at the threshold value: resolved by page index
+        vals = torch.randint(0, 3, shape, generator=g)
+    elif kind == "wide-integers":  # negative and positive scores, scattered small ties
+        vals = torch.randint(-2048, 2049, shape, generator=g)
+    else:  # "planted-ties": 40 candidates share the value just inside the top-k
+        vals = torch.randint(0, 2048, shape, generator=g)
+        P = -(-int(inp.seq_lens[0]) // w.page_size)
+        k_top = n_sel - w.n_sink - w.n_recent
+        for h in range(w.num_kv_heads):
+            phys = inp.page_table[0, w.n_sink:P - w.n_recent].cpu().long()
+            cand = vals[phys, h]
+            v = int(torch.sort(cand, descending=True).values[k_top - 15])
+            pick = torch.randperm(len(phys), generator=g)[:40]
+            vals[phys[pick], h] = v
+    inp.k_pool.zero_()
+    inp.k_pool[..., 0] = vals[:, :, None].to(device=DEV, dtype=inp.k_pool.dtype)
+    inp.q.zero_()
+    inp.q[..., 0] = 1
+    return w, inp
+
+
+@pytest.mark.parametrize("kind", ["three-values", "planted-ties", "wide-integers"])
+def test_exact_ties_across_the_cluster(kind):
+    """Exact ties between pages scored in different CTAs: lower page index wins."""
+    w, inp = _integer_score_inputs(kind)
+    p, bufs, err = run_step(inp)
+    assert err == 0
+    prm = oracle_params(w)
+    for h in range(w.num_kv_heads):
+        sub = unit_inputs(inp, 0, h)
+        scores = decode.unit_scores(sub, prm, 0, 0)
+        P = -(-int(inp.seq_lens[0]) // w.page_size)
+        ref = oselect.select_pages(scores, P, prm.n_sel, prm.n_sink, prm.n_recent)
+        assert gpu_selection(bufs, 0, h) == ref
+        check_unit(inp, prm, bufs, 0, h, TOL_OUT[w.kv_dtype])
+
+
+def test_budget_of_only_forced_pages():
+    """A budget equal to the forced pages selects no candidate."""
+    w = scaled(SMALL["mha"], n_sel_pages=2)
+    inp = make_inputs(w, device=DEV)
+    p, bufs, err = run_step(inp)
+    assert err == 0
+    P = -(-int(inp.seq_lens[0]) // w.page_size)
+    prm = oracle_params(w)
+    for h in range(w.num_kv_heads):
+        assert gpu_selection(bufs, 0, h) == [0, P - 1]
+        check_unit(inp, prm, bufs, 0, h, TOL_OUT[w.kv_dtype])
 
 
 @pytest.mark.parametrize("name", ["tiny", "long-d64-g8"])
