@@ -399,12 +399,23 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
         for (int g = 1; g < G; ++g) s = __fadd_rn(s, to_f32(qb[g * D + i]));
         s_qbar[i] = __fdiv_rn(s, static_cast<float>(G));
       }
-      for (int i = threadIdx.x; i < D * DS; i += CW * 32) s_P[i] = a.proj[i];
+      {  // P (16-byte aligned): all of a thread's loads in flight at once
+        constexpr int NV = D * DS / 4 / (CW * 32);
+        const float4* P4 = reinterpret_cast<const float4*>(a.proj);
+        float4 v[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) v[u] = __ldg(P4 + threadIdx.x + u * CW * 32);
+#pragma unroll
+        for (int u = 0; u < NV; ++u) reinterpret_cast<float4*>(s_P)[threadIdx.x + u * CW * 32] = v[u];
+      }
       consumers_sync();
       if (warp == 0) {
         float qt = 0.f;
-        if (lane < DS)
+        if (lane < DS) {
+          // products in any order, the sum in channel order
+#pragma unroll 16
           for (int i = 0; i < D; ++i) qt = __fadd_rn(qt, __fmul_rn(s_qbar[i], s_P[i * DS + lane]));
+        }
         float am = fabsf(qt);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -441,15 +452,18 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
             cz[r] = r < nb ? __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r0 + r]), a.inv_sqrt_d)
                            : 0.f;
           sketch_block_scores4(st + r0 * rb, rb, nb, S, qc, cz, score);
-          if (lane == 0) {
+          // every lane holds the four scores: lane r sends block r's key
+          // (one remote store instruction for the four)
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-              if (r < nb) {
-                const uint32_t k0 = score_key(score[r]);
-                st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r0 + r - lo), k0);
-                kmn = min(kmn, k0);
-                kmx = max(kmx, k0);
-              }
+          for (int r = 0; r < 4; ++r)
+            if (r < nb) {
+              const uint32_t k0 = score_key(score[r]);
+              kmn = min(kmn, k0);
+              kmx = max(kmx, k0);
+            }
+          if (lane < nb) {
+            const float sc = lane == 0 ? score[0] : lane == 1 ? score[1] : lane == 2 ? score[2] : score[3];
+            st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r0 + lane - lo), score_key(sc));
           }
         }
         __syncwarp();
@@ -551,7 +565,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       for (int s0 = 0; s0 < nb && ok; s0 += PPS) {
         const int k = n_scan + (base + s0) / PPS, stage = k % STAGES;
         bool lok = true;
-        if (lane == 0 && k >= STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
+        // a slot's previous use was a scan stage for the first STAGES attend
+        // stages: all of those were consumed before the scan's cluster barrier
+        if (lane == 0 && k >= n_scan + STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
         if (!lok) record_error(a.err, SPG_DEVERR_TIMEOUT);
         ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0;
         if (!ok) break;

@@ -569,13 +569,27 @@ __device__ __forceinline__ void quest_query(const T* qrows, int hl, float (&qf)[
   }
 }
 
-// int4 nibbles of one 32-bit word -> two words of 4 signed int8 lanes
-// (even-index codes, odd-index codes)
-__device__ __forceinline__ void unpack_int4x8(uint32_t w, int& even, int& odd) {
+// acc + the dot product of the 8 int4 codes of w (two's-complement nibbles;
+// even-index codes in the low nibbles) with int8 query codes (q_even, q_odd:
+// 4 bytes each), except that every code c enters as c + 8: the nibble with
+// its top bit flipped is c + 8 in 0..15, an unsigned byte, so a mask, a shift
+// and an XOR replace the sign extension.  The caller subtracts
+// sketch_query_bias() once per token: the result is then the exact integer
+// dot product.
+__device__ __forceinline__ int dot_int4x8_biased(uint32_t w, int q_even, int q_odd, int acc) {
   const uint32_t lo = (w & 0x0f0f0f0fu) ^ 0x08080808u;
   const uint32_t hi = ((w >> 4) & 0x0f0f0f0fu) ^ 0x08080808u;
-  even = static_cast<int>(__vsub4(lo, 0x08080808u));
-  odd = static_cast<int>(__vsub4(hi, 0x08080808u));
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(lo), "r"(q_even));
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(hi), "r"(q_odd));
+  return acc;
+}
+// 8 times the sum of the 16 query codes packed in qc[4]: what the +8 of every
+// key code adds to a token's biased dot product
+__device__ __forceinline__ int sketch_query_bias(const int* qc) {
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s = __dp4a(qc[k], 0x01010101, s);
+  return 8 * s;
 }
 
 __device__ __forceinline__ int pack_i8x4(int a, int b, int c, int d) {
@@ -629,19 +643,15 @@ __device__ void sketch_index_query(const TQ* qb, int G, int d, const float* proj
 __device__ __forceinline__ float sketch_block_score(const uint2 (&wk)[4], int S, const int* qc,
                                                     float cz) {
   const int lane = threadIdx.x & 31;
+  const int bias = sketch_query_bias(qc);
   float zmax = -INFINITY;
   float z[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     z[k] = -INFINITY;
     if (lane + 32 * k < S) {
-      int e0, o0, e1, o1;
-      unpack_int4x8(wk[k].x, e0, o0);
-      unpack_int4x8(wk[k].y, e1, o1);
-      int dot = __dp4a(e0, qc[0], 0);
-      dot = __dp4a(o0, qc[1], dot);
-      dot = __dp4a(e1, qc[2], dot);
-      dot = __dp4a(o1, qc[3], dot);
+      int dot = dot_int4x8_biased(wk[k].x, qc[0], qc[1], -bias);
+      dot = dot_int4x8_biased(wk[k].y, qc[2], qc[3], dot);
       z[k] = static_cast<float>(dot) * cz;
       zmax = fmaxf(zmax, z[k]);
     }
@@ -664,6 +674,7 @@ __device__ __forceinline__ void sketch_block_scores4(const uint8_t* tile, int rb
                                                      float (&score)[4]) {
   const int lane = threadIdx.x & 31;
   constexpr float kL2e = 1.4426950408889634f;
+  const int bias = sketch_query_bias(qc);
   float z[4][4], zmax[4];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -673,13 +684,8 @@ __device__ __forceinline__ void sketch_block_scores4(const uint8_t* tile, int rb
       z[r][k] = -INFINITY;
       if (r < nb && lane + 32 * k < S) {
         const uint2 w = *reinterpret_cast<const uint2*>(tile + r * rb + (lane + 32 * k) * 8);
-        int e0, o0, e1, o1;
-        unpack_int4x8(w.x, e0, o0);
-        unpack_int4x8(w.y, e1, o1);
-        int dot = __dp4a(e0, qc[0], 0);
-        dot = __dp4a(o0, qc[1], dot);
-        dot = __dp4a(e1, qc[2], dot);
-        dot = __dp4a(o1, qc[3], dot);
+        int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
+        dot = dot_int4x8_biased(w.y, qc[2], qc[3], dot);
         z[r][k] = static_cast<float>(dot) * cz[r] * kL2e;  // log2 domain
         zmax[r] = fmaxf(zmax[r], z[r][k]);
       }
