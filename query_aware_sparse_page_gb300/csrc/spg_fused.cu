@@ -545,89 +545,71 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   cluster_sync();  // every CTA has its slice of the selection
 
   // ---------------------------------------------------------------- attend
+  // Attend stage j holds pages [j * PPS, (j + 1) * PPS) of this CTA's slice;
+  // stages are numbered on from the scan's (k = n_scan + j) and stage k
+  // belongs to consumer warp k % CW, which issues its copies itself, keeps up
+  // to STAGES / CW of its stages in flight and refills a slot as soon as it
+  // has consumed it (a slot always has the same owner, so no handshake sits
+  // between the consumer and the next copy into its slot).
   const int n_att = s_natt;
   Consumer cons;
-  if (warp == CW) {
-    const T* kpool = static_cast<const T*>(a.k_pool);
-    const T* vpool = static_cast<const T*>(a.v_pool);
+  if (warp < CW) {
+    cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
+              a.scale_log2, warp, lane);
     const uint32_t tile = static_cast<uint32_t>(S) * D * sizeof(T);
     const uint32_t scb = is_i8<T>() ? static_cast<uint32_t>(S) * 2 : 0u;
     const uint64_t pol = policy_evict_first();
-    for (int base = 0; base < n_att && ok; base += 32) {
-      int ph = -1, nv = 0;
-      const int j = base + lane;
-      if (j < n_att) {
-        ph = s_att_ph[j];
-        nv = s_att_nv[j];
-      }
-      // one stage at a time: PPS pages, one lane each
-      const int nb = min(32, n_att - base);
-      for (int s0 = 0; s0 < nb && ok; s0 += PPS) {
-        const int k = n_scan + (base + s0) / PPS, stage = k % STAGES;
-        bool lok = true;
-        // a slot's previous use was a scan stage for the first STAGES attend
-        // stages: all of those were consumed before the scan's cluster barrier
-        if (lane == 0 && k >= n_scan + STAGES) lok = mbar_wait_bounded(&empty[stage], ((k / STAGES) - 1) & 1);
-        if (!lok) record_error(a.err, SPG_DEVERR_TIMEOUT);
-        ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const int np = min(PPS, nb - s0);
-        if (lane >= s0 && lane < s0 + np) {
-          const int i = lane - s0;
-          uint8_t* dst = ring + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes;
-          s_nv[stage * kMaxPagesPerStage + i] = ph >= 0 ? nv : 0;
-          if (ph >= 0) {
-            const size_t row = static_cast<size_t>(ph) * Hkv + h;
-            mbar_expect_tx(&full[stage], 2 * tile + 2 * scb);
-            if constexpr (MMA) {
+    const int n_st = (n_att + PPS - 1) / PPS;
+    auto issue = [&](int j) {
+      const int k = n_scan + j, stage = k % STAGES;
+      const int np = min(PPS, n_att - j * PPS);
+      if (lane < np) {
+        const int ph = s_att_ph[j * PPS + lane];
+        uint8_t* dst = ring + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(lane) * pbytes;
+        s_nv[stage * kMaxPagesPerStage + lane] = ph >= 0 ? s_att_nv[j * PPS + lane] : 0;
+        if (ph >= 0) {
+          const size_t row = static_cast<size_t>(ph) * Hkv + h;
+          mbar_expect_tx(&full[stage], 2 * tile + 2 * scb);
+          if constexpr (MMA) {
+            const int y = static_cast<int>(row) * S;
+            if (a.whole_page) {
+              tma_load_3d(dst, &a.tmk, 0, y, 0, &full[stage], pol);
+              tma_load_3d(dst + tile, &a.tmv, 0, y, 0, &full[stage], pol);
+            } else {
               // swizzled tiles of [S rows][128 bytes] for K, then for V
               constexpr int NT = D * static_cast<int>(sizeof(T)) / 128, EPT = 128 / sizeof(T);
-              const int y = static_cast<int>(row) * S;
-              if (a.whole_page) {
-                tma_load_3d(dst, &a.tmk, 0, y, 0, &full[stage], pol);
-                tma_load_3d(dst + tile, &a.tmv, 0, y, 0, &full[stage], pol);
-              } else {
 #pragma unroll
-                for (int hf = 0; hf < NT; ++hf) {
-                  tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
-                  tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
-                }
-              }
-              if constexpr (is_i8<T>()) {
-                bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
-                bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
-              }
-            } else {
-              bulk_g2s_hint(dst, kpool + row * S * D, tile, &full[stage], pol);
-              bulk_g2s_hint(dst + tile, vpool + row * S * D, tile, &full[stage], pol);
-              if constexpr (is_i8<T>()) {
-                bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
-                bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
+              for (int hf = 0; hf < NT; ++hf) {
+                tma_load_2d(dst + hf * S * 128, &a.tmk, hf * EPT, y, &full[stage], pol);
+                tma_load_2d(dst + tile + hf * S * 128, &a.tmv, hf * EPT, y, &full[stage], pol);
               }
             }
+          } else {
+            bulk_g2s_hint(dst, static_cast<const T*>(a.k_pool) + row * S * D, tile, &full[stage], pol);
+            bulk_g2s_hint(dst + tile, static_cast<const T*>(a.v_pool) + row * S * D, tile, &full[stage], pol);
+          }
+          if constexpr (is_i8<T>()) {
+            bulk_g2s(dst + 2 * tile, a.k_scale + row * S, scb, &full[stage]);
+            bulk_g2s(dst + 2 * tile + scb, a.v_scale + row * S, scb, &full[stage]);
           }
         }
-        if (lane == 0) s_np[stage] = np;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[stage]);
       }
-    }
-    if (!ok && lane == 0) {
-      // drain the copies this producer may still have in flight before the ring is reused
-      // (bounded waits; uses that were never issued simply time out)
-      const int issued = n_scan + (n_att + PPS - 1) / PPS;
-      for (int k = max(0, issued - STAGES); k < issued; ++k)
-        mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
-    }
-  } else if (warp < CW) {
-    cons.init(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D,
-              a.scale_log2, warp, lane);
-    const int n_att_st = (n_att + PPS - 1) / PPS;
-    // this warp's attention stages: k = n_scan + ka with k % CW == warp
-    const int ka0 = ((warp - n_scan) % CW + CW) % CW;
-    for (int ka = ka0; ka < n_att_st && ok; ka += CW) {
-      const int k = n_scan + ka, stage = k % STAGES;
+      __syncwarp();
+      if (lane == 0) {
+        s_np[stage] = np;
+        mbar_arrive(&full[stage]);
+      }
+    };
+    // this warp's slots last held scan stages it consumed (generic-proxy
+    // reads) before the asynchronous copies that now land there
+    fence_proxy_async();
+    const int j0 = ((warp - n_scan) % CW + CW) % CW;
+    int nxt = j0;  // the next of this warp's stages not yet issued
+    for (int j = j0; ok && j < n_st; j += CW) {
+      for (; nxt < n_st && nxt < j + STAGES; nxt += CW) issue(nxt);
+      const int k = n_scan + j, stage = k % STAGES;
       if (!mbar_wait_bounded(&full[stage], (k / STAGES) & 1)) {
+        ok = false;
         if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
         break;
       }
@@ -642,9 +624,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
             cons.consume(pg, S, nv);
         }
       }
-      if constexpr (MMA) fence_proxy_async();  // zeroed slots before the next TMA write
+      fence_proxy_async();  // reads (and zeroed slots) before the next copy into the slot
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    if (!ok && lane == 0) {
+      // wait (bounded) for the copies this warp may still have in flight
+      for (int j = max(j0, nxt - STAGES); j < nxt; j += CW) {
+        const int k = n_scan + j;
+        mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
+      }
     }
     cons.fold();
   }
