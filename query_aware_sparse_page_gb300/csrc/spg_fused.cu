@@ -80,6 +80,7 @@ struct FusedArgs {
   int Hkv, S, MP, n_phys, n_sink, n_recent, n_sel, stages, rows_per_stage, append;
   int cluster, pages_per_stage;
   uint32_t stage_bytes, row_bytes, page_bytes, ring_bytes, keys_off, sel_off, att_off;
+  uint32_t pt_off;  // leader: the unit's page-table row, when it fits (0: not cached)
   float scale_log2, inv_sqrt_d;
 };
 
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   __shared__ float s_P[SEL ? 256 * 16 : 1];
   __shared__ int s_qc[4];
   __shared__ float s_sq;
+  __shared__ __align__(8) uint64_t s_ptbar;  // leader: the page-table row has landed
   __shared__ int s_natt;  // pages of the selection this CTA attends to
   __shared__ float s_samax[kMaxCluster];  // sketch append: each CTA's |max|
   float sk_v[SEL ? kSketchVals : 1];       // sketch append: this lane's projected values
@@ -266,6 +268,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   uint32_t* s_mm = reinterpret_cast<uint32_t*>(smem + a.att_off);         // leader: [2][C*CW] key min/max
   int* s_att_ph = reinterpret_cast<int*>(s_mm + 2 * kMaxCluster * CW);    // [n_sel] physical pages
   int* s_att_nv = s_att_ph + a.n_sel;                                     // [n_sel] valid tokens
+  int* s_pt = reinterpret_cast<int*>(smem + a.pt_off);                    // leader: page-table row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -280,6 +283,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    mbar_init(&s_ptbar, 1);
     mbar_fence_init();
   }
   if constexpr (MMA) {
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   bool ok = true;
 
   if (warp == CW) {
-    if (rank == C - 1 && lane == 0 && P > 0) {
+    if (a.pt_off == 0 && rank == C - 1 && lane == 0 && P > 0) {
       // the attend phase looks the selected pages up in this row: have it in
       // L2 by then
       const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.MP;
@@ -344,6 +348,18 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     // auxiliary warp: the metadata append of the token at L-1.  Its page is
     // forced (n_recent >= 1), so neither this step's scan nor its attend
     // reads that metadata; done here it overlaps the scan.
+    if (a.pt_off != 0 && rank == 0 && lane == 0) {
+      // the leader looks the selected pages up in this row: one bulk copy of
+      // its first P entries (rounded up to 16 bytes, within the row: the
+      // host caches only rows of a multiple of 4 entries) lands it in shared
+      // memory during the scan
+      const uint32_t bytes = (static_cast<uint32_t>(P) * 4u + 15u) & ~15u;
+      if (bytes > 0) {
+        mbar_expect_tx(&s_ptbar, bytes);
+        bulk_g2s(s_pt, a.page_table + static_cast<size_t>(b) * a.MP, bytes, &s_ptbar);
+      }
+      mbar_arrive(&s_ptbar);
+    }
     if constexpr (SEL == 0) {
       if (a.append && rank == C - 1 && L > 0) append_minmax_warp<T, D>(a, b, h, L, lane);
     } else {
@@ -510,6 +526,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       block_topk(s_keys, nc, k_top, lo, s_sel + lo, tk, true, true);
     }
     __syncthreads();
+    if (a.pt_off != 0 && !mbar_wait_bounded(&s_ptbar, 0) && tid == 0)
+      record_error(a.err, SPG_DEVERR_TIMEOUT);
     // the selection to HBM, and each CTA's slice of it (physical page, valid
     // tokens) into that CTA's shared memory, so that its attend phase starts
     // from local data
@@ -523,7 +541,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
         if (lp < 0 || lp >= P) {
           record_error(a.err, SPG_DEVERR_SEL);
         } else {
-          ph = a.page_table[static_cast<size_t>(b) * a.MP + lp];
+          ph = a.pt_off != 0 ? s_pt[lp] : a.page_table[static_cast<size_t>(b) * a.MP + lp];
           if (ph < 0 || ph >= a.n_phys) {
             record_error(a.err, SPG_DEVERR_PAGE_ID);
             ph = -1;
@@ -707,7 +725,7 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   const size_t att_off = (sel_off + sizeof(int) * n_sel_pages(p) + 127) & ~static_cast<size_t>(127);
   const size_t att_bytes = sizeof(uint32_t) * 2 * kMaxCluster * kConsumerWarps +
                            sizeof(int) * 2 * n_sel_pages(p);
-  const size_t smem = 1024 + att_off + att_bytes;  // + alignment slack
+  size_t smem = 1024 + att_off + att_bytes;  // + alignment slack
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
   if constexpr (MMA) {
     const long long rows = static_cast<long long>(p.num_phys_pages) * p.num_kv_heads * S;
@@ -740,6 +758,20 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
+  // the leader's copy of the page-table row, when it costs no occupancy (and
+  // rows are 16-byte aligned for the bulk copy)
+  a.pt_off = 0;
+  if (p.max_pages_per_seq % 4 == 0) {
+    const size_t pt_off = (smem - 1024 + 127) & ~static_cast<size_t>(127);
+    const size_t smem_pt = 1024 + pt_off + sizeof(int) * p.max_pages_per_seq;
+    int per_sm_pt = 0;
+    if (smem_pt <= 227u * 1024u && ensure_smem(kern, smem_pt) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_pt, kern, threads, smem_pt) == cudaSuccess &&
+        per_sm_pt >= per_sm) {
+      a.pt_off = static_cast<uint32_t>(pt_off);
+      smem = smem_pt;
+    }
+  }
   const int slots = device_sm_count() * per_sm;
   int C = kMaxCluster;
   while (C > 2 && units * C > slots) C /= 2;
