@@ -204,6 +204,34 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
   const int nw = nt >> 5;
   const int n16 = n & ~15;  // keys in whole 16-key runs; the tail is read one by one
   SPG_TK_MARK(t, 0);
+  if (n <= nt) {
+    // Few keys: thread i ranks key i by counting the keys that come before it
+    // in the total order (key descending, index ascending); the ranks are a
+    // permutation of 0 .. n-1 and rank < k is the top-k.  One block scan of
+    // the chosen flags gives the ascending positions.
+    int r = 0;
+    if (tid < n) {
+      const uint32_t x = keys[tid];
+      const int n4 = n & ~3;
+      for (int j = 0; j < n4; j += 4) {
+        const uint4 y = *reinterpret_cast<const uint4*>(keys + j);  // the same 16 bytes for the whole warp
+        r += (y.x > x) || (y.x == x && j < tid);
+        r += (y.y > x) || (y.y == x && j + 1 < tid);
+        r += (y.z > x) || (y.z == x && j + 2 < tid);
+        r += (y.w > x) || (y.w == x && j + 3 < tid);
+      }
+      for (int j = n4; j < n; ++j) {
+        const uint32_t y = keys[j];
+        r += (y > x) || (y == x && j < tid);
+      }
+    }
+    const bool chosen = tid < n && r < k;
+    const int pos = block_exclusive_scan(chosen ? 1 : 0, t.wa, &t.total);
+    if (chosen) dst[pos] = base + tid;
+    __syncthreads();
+    SPG_TK_MARK(t, 7);
+    return;
+  }
   if (!minmax_ready) {
     uint32_t mn = 0xffffffffu, mx = 0u;
     for (int r = tid; r * 16 < n16; r += nt) {  // runs 64 B apart: rotate by r / 2
