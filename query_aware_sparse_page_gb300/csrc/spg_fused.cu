@@ -450,6 +450,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       }
       consumers_sync();
       const int qc[4] = {s_qc[0], s_qc[1], s_qc[2], s_qc[3]};
+      const int qbias = sketch_query_bias(qc);
       const float sq = s_sq;
       for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
@@ -460,27 +461,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
         }
         const int nr = min(R, rows - ks * R);
         const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
-        for (int r0 = 0; r0 < nr; r0 += 4) {  // the stage's blocks, four at a time
-          const int nb = min(4, nr - r0);
-          float cz[4], score[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            cz[r] = r < nb ? __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + r0 + r]), a.inv_sqrt_d)
-                           : 0.f;
-          sketch_block_scores4(st + r0 * rb, rb, nb, S, qc, cz, score);
-          // every lane holds the four scores: lane r sends block r's key
-          // (one remote store instruction for the four)
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (r < nb) {
-              const uint32_t k0 = score_key(score[r]);
-              kmn = min(kmn, k0);
-              kmx = max(kmx, k0);
-            }
-          if (lane < nb) {
-            const float sc = lane == 0 ? score[0] : lane == 1 ? score[1] : lane == 2 ? score[2] : score[3];
-            st_cluster_u32(keys_leader + 4u * (c0 + ks * R + r0 + lane - lo), score_key(sc));
-          }
+        // the stage's blocks (nr <= 32), one per lane; every scored block is
+        // full (the open tail block is forced, never scored)
+        if (lane < nr) {
+          const float cz = __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + lane]), a.inv_sqrt_d);
+          const float sc = sketch_block_score_lane(st + lane * rb, S, qc, qbias, cz);
+          const uint32_t k0 = score_key(sc);
+          st_cluster_u32(keys_leader + 4u * (c0 + ks * R + lane - lo), k0);
+          kmn = min(kmn, k0);
+          kmx = max(kmx, k0);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
@@ -780,7 +769,8 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   // stage of the CTA's chunk of blocks (the stage buffers stay as planned)
   if (p.selector == SPG_SEL_SKETCH_INT4) {
     const int cpc_max = (p.max_pages_per_seq + C - 1) / C;
-    a.rows_per_stage = std::min(R, std::max(4, (cpc_max + kConsumerWarps - 1) / kConsumerWarps));
+    // (at most 32: a warp scores one block per lane)
+    a.rows_per_stage = std::min(std::min(R, 32), std::max(4, (cpc_max + kConsumerWarps - 1) / kConsumerWarps));
   }
   // the sketch append gives each aux-warp lane one token of the block
   if (a.append && p.selector == SPG_SEL_SKETCH_INT4 && S > C * 32)

@@ -9,6 +9,7 @@
 // 确定性红线): see block_topk.
 #pragma once
 
+#include <climits>
 #include <float.h>
 
 #include "spg_common.cuh"
@@ -213,6 +214,7 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     if (tid < n) {
       const uint32_t x = keys[tid];
       const int n4 = n & ~3;
+#pragma unroll 4
       for (int j = 0; j < n4; j += 4) {
         const uint4 y = *reinterpret_cast<const uint4*>(keys + j);  // the same 16 bytes for the whole warp
         r += (y.x > x) || (y.x == x && j < tid);
@@ -737,6 +739,40 @@ __device__ __forceinline__ void sketch_block_scores4(const uint8_t* tile, int rb
     for (int r = 0; r < 4; ++r) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
 #pragma unroll
   for (int r = 0; r < 4; ++r) score[r] = (zmax[r] + log2f(sum[r])) * kLn2;
+}
+
+// Score of one full sketch block (S tokens x 8 bytes of int4 codes at blk)
+// for one lane: z_t = dot(codes_t, qc) * cz, score = max z + ln sum exp(z -
+// max z), without any exchange between lanes, so that a warp scores up to 32
+// blocks at once (lane r taking block r).  Lane r reads token (t + r) mod S
+// at step t: the eight-byte reads of a half-warp then fall in different bank
+// pairs.  cz > 0 (a product of positive scales), so the maximum logit is cz
+// times the maximum integer dot, exactly; a second pass sums exp2 in the log2
+// domain.
+__device__ __forceinline__ float sketch_block_score_lane(const uint8_t* blk, int S, const int* qc,
+                                                         int bias, float cz) {
+  constexpr float kL2e = 1.4426950408889634f;
+  const int rot = threadIdx.x & 31;
+  int dmax = INT_MIN;
+  for (int t = 0; t < S; ++t) {
+    int tt = t + rot;
+    if (tt >= S) tt -= S;
+    const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
+    int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
+    dot = dot_int4x8_biased(w.y, qc[2], qc[3], dot);
+    dmax = max(dmax, dot);
+  }
+  const float zmax = static_cast<float>(dmax) * cz * kL2e;
+  float sum = 0.f;
+  for (int t = 0; t < S; ++t) {
+    int tt = t + rot;
+    if (tt >= S) tt -= S;
+    const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
+    int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
+    dot = dot_int4x8_biased(w.y, qc[2], qc[3], dot);
+    sum += exp2f(static_cast<float>(dot) * cz * kL2e - zmax);
+  }
+  return (zmax + log2f(sum)) * kLn2;
 }
 
 }  // namespace spg
