@@ -41,9 +41,9 @@ NOMINAL_HBM_GBS = 8000.0
 # that workload, and the sha256 of the kernel sources it was taken on
 # (profiles/k_fused_<workload>.md).  Reported only while the sources match.
 NCU_TRAFFIC = {
-    "llama2-7b-mha-32k": (67_875_072, "2cb638e6d808c8c4e543a3cc13e91aea35d855ed674fdb5094a7aa853d64ba36"),
-    "long-scan-b4-128k": (205_324_288, "2cb638e6d808c8c4e543a3cc13e91aea35d855ed674fdb5094a7aa853d64ba36"),
-    "sals-int8-b16-10k-4x": (100_482_560, "2cb638e6d808c8c4e543a3cc13e91aea35d855ed674fdb5094a7aa853d64ba36"),
+    "llama2-7b-mha-32k": (67_790_848, "78fb4828674717310eb359925fdef0bdbf61b99311e1807a7c372f89a9a23988"),
+    "long-scan-b4-128k": (205_888_768, "78fb4828674717310eb359925fdef0bdbf61b99311e1807a7c372f89a9a23988"),
+    "sals-int8-b16-10k-4x": (100_546_816, "78fb4828674717310eb359925fdef0bdbf61b99311e1807a7c372f89a9a23988"),
 }
 
 
