@@ -38,25 +38,33 @@ NOMINAL_HBM_GBS = 8000.0
 
 # ---------------------------------------------------------------------------- utils
 # DRAM bytes (read + write) of one k_fused launch, from one ncu capture of
-# that workload, and the sha256 of the kernel sources it was taken on
-# (profiles/k_fused_<workload>.md).  Reported only while the sources match.
+# that workload, and the sha256 of the kernel code it was taken on (see
+# csrc_sha256; profiles/k_fused_<workload>.md).  Reported only while the code
+# matches.
 NCU_TRAFFIC = {
-    "llama2-7b-mha-32k": (67_790_848, "78fb4828674717310eb359925fdef0bdbf61b99311e1807a7c372f89a9a23988"),
-    "long-scan-b4-128k": (205_888_768, "78fb4828674717310eb359925fdef0bdbf61b99311e1807a7c372f89a9a23988"),
-    "sals-int8-b16-10k-4x": (100_546_816, "78fb4828674717310eb359925fdef0bdbf61b99311e1807a7c372f89a9a23988"),
+    "llama2-7b-mha-32k": (67_790_848, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a"),
+    "long-scan-b4-128k": (205_888_768, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a"),
+    "sals-int8-b16-10k-4x": (100_546_816, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a"),
 }
 
 
 def csrc_sha256() -> str:
+    """sha256 over the kernel sources (sorted by name; name, then the text with
+    // and /* */ comments removed and whitespace runs collapsed): the code an
+    ncu capture was taken on."""
     import hashlib
+    import re
 
     d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "query_aware_sparse_page_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                code = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+            code = re.sub(r"//[^\n]*", "", code)
+            code = " ".join(code.split())  # whitespace runs as one space
             h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+            h.update(code.encode())
     return h.hexdigest()
 
 

@@ -10,30 +10,35 @@
 // indices never leave the chip here, they cross shared memory).
 //
 // Phases of one cluster (every CTA has 4 consumer warps, 1 producer warp and
-// 1 auxiliary warp;
-// each ring stage has one owner warp, stage k belonging to warp k % 4):
+// 1 auxiliary warp; each ring stage has one owner warp, stage k belonging to
+// warp k % 4):
 //  1. scan: the unit's candidate pages are split into contiguous chunks, one
 //     per CTA.  Metadata is stored per sequence in logical page order, so a
 //     chunk's rows (Quest: m and M, 2*d elements; sketch: the block's int4
 //     codes) are one contiguous range; the producer streams it into the
 //     shared-memory ring with one cp.async.bulk per stage of up to 64 rows.
 //     Quest rows are scored 16 pages per tensor-core tile (A = the rows,
-//     B = [q-; q+] for the group's query rows), sketch blocks by int8 dots.
-//     Each order-preserving key goes straight into the leader CTA's shared
-//     memory (st.shared::cluster), and each warp reports its keys' min / max.
+//     B = [q-; q+] for the group's query rows); sketch blocks one per lane
+//     by int4 x int8 dots and a log-sum-exp.  Each order-preserving key goes
+//     straight into the leader CTA's shared memory (st.shared::cluster), and
+//     each warp reports its keys' min / max.
 //  2. cluster barrier; the leader (rank 0) runs the exact top-k over the
 //     keys, adds the forced pages, writes sel / sel_cnt, and pushes each
 //     CTA's slice of the selection (physical page, valid tokens) into that
 //     CTA's shared memory; cluster barrier.
-//  3. attend: each CTA's producer copies its pages' K/V tiles into the ring
-//     (fp16/bf16: 2-D TMA tiles with 128-byte swizzle for the tensor-core
-//     consumer; int8: bulk copies with their scales for the CUDA-core
-//     consumer); the CTA's partial (m, l, acc) per query row goes into the
-//     leader's shared memory.
+//  3. attend: each consumer warp copies the K/V pages of its own ring stages
+//     (fp16/bf16, and int8 with d = 128 and an fp16 query: one 3-D TMA copy
+//     per page for K and for V, landing as 128-byte-swizzled tiles for the
+//     tensor-core consumers; other int8 shapes: bulk copies for the CUDA-core
+//     consumer; int8 scales by bulk copy) and refills a stage as soon as it
+//     has consumed it; the CTA's partial (m, l, acc) per query row goes into
+//     the leader's shared memory.
 //  4. cluster barrier; the leader merges the partials and writes out / lse.
 // An auxiliary warp of the last CTA applies the metadata append of the new
 // token during the scan (Quest min/max of its page; the sketch of a block it
-// completes): that page is forced, so nothing in the step reads it.
+// completes, split over every CTA's auxiliary warp): that page is forced, so
+// nothing in the step reads it.  The leader's auxiliary warp bulk-copies the
+// unit's page-table row into shared memory when it fits.
 // No CTA waits on another except at the three hardware cluster barriers,
 // which every thread of every CTA reaches on every path; all mbarrier waits
 // are bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still
