@@ -48,14 +48,15 @@ NCU_TRAFFIC = {
 }
 
 
-def csrc_sha256() -> str:
-    """sha256 over the kernel sources (sorted by name; name, then the text with
-    // and /* */ comments removed and whitespace runs collapsed): the code an
-    ncu capture was taken on."""
+def csrc_sha256(d: str | None = None) -> str:
+    """sha256 over the kernel sources in d (the package's csrc/ by default;
+    sorted by name; name, then the text with // and /* */ comments removed and
+    whitespace runs collapsed): the code an ncu capture was taken on."""
     import hashlib
     import re
 
-    d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "query_aware_sparse_page_gb300", "csrc")
+    if d is None:
+        d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "query_aware_sparse_page_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh", ".h")):
