@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <type_traits>
 #include <utility>
 
@@ -335,27 +336,42 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // Raises a kernel's dynamic shared-memory limit when its static plus dynamic
-// shared memory exceeds the default 48 KB (once per kernel and size;
-// repeated calls are no-ops).
+// shared memory exceeds the default 48 KB.  The attribute belongs to the
+// current device, so the cache of what was raised is keyed by (device,
+// kernel) and guarded by a lock: host threads may launch concurrently and
+// one thread may drive several GPUs.  Repeated calls are no-ops.
 template <typename... KArgs>
 inline cudaError_t ensure_smem(void (*kern)(KArgs...), size_t bytes) {
   struct Entry {
+    int dev;
     const void* fn;
     size_t bytes;
   };
-  static Entry cache[128];
+  static Entry cache[256];
   static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   const void* fn = reinterpret_cast<const void*>(kern);
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n; ++i)
-    if (cache[i].fn == fn && cache[i].bytes >= bytes) return cudaSuccess;
+    if (cache[i].dev == dev && cache[i].fn == fn && cache[i].bytes >= bytes) return cudaSuccess;
   cudaFuncAttributes attr{};
-  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.sharedSizeBytes + bytes > 48 * 1024)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes));
-  if (e == cudaSuccess && n < 128) cache[n++] = Entry{fn, bytes};
-  return e;
+  if (e != cudaSuccess) return e;
+  int i = 0;
+  while (i < n && !(cache[i].dev == dev && cache[i].fn == fn)) ++i;
+  if (i < n) {
+    cache[i].bytes = bytes > cache[i].bytes ? bytes : cache[i].bytes;
+  } else if (n < 256) {
+    cache[n++] = Entry{dev, fn, bytes};
+  }
+  return cudaSuccess;
 }
 
 // Quest metadata row layout: a row holds m (d channels) then M (d channels)
@@ -370,9 +386,11 @@ __host__ __device__ __forceinline__ int meta_swz(int e, int p) {
   return ((e / EPC) ^ (p & 7)) * EPC + (e % EPC);
 }
 
-// order-preserving map of an fp32 score to uint32 (larger float -> larger key)
+// order-preserving map of an fp32 score to uint32 (larger float -> larger key);
+// -0 is first turned into +0 (-0 + +0 = +0 when rounding to nearest), so that
+// the two zeros, equal as values, get one key and tie by page index
 __device__ __forceinline__ uint32_t score_key(float s) {
-  uint32_t u = __float_as_uint(s);
+  uint32_t u = __float_as_uint(__fadd_rn(s, 0.0f));
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

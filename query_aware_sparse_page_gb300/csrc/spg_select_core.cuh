@@ -99,19 +99,6 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_t
 }
 
 // Shared state of the block top-k for up to MAXN keys.
-#ifdef SPG_TOPK_PROFILE
-__device__ int g_topk_stop;
-#define SPG_TK_MARK(t, i) \
-  do {                    \
-    if (threadIdx.x == 0) (t).marks[i] = clock64(); \
-    if (g_topk_stop == (i)) { __syncthreads(); return; } \
-  } while (0)
-#else
-#define SPG_TK_MARK(t, i) \
-  do {                    \
-  } while (0)
-#endif
-
 // 16-byte aligned: the histogram is cleared and read with 16-byte accesses
 template <int MAXN>
 struct alignas(16) TopkSmem {
@@ -127,11 +114,6 @@ struct alignas(16) TopkSmem {
   uint32_t candk[256];  // and their keys
   uint32_t gtw[kWords];  // bitmap: keys above the threshold
   uint32_t eqw[kWords];  // bitmap: keys in the threshold bucket (or equal to the threshold)
-#ifdef SPG_TOPK_PROFILE
-  long long marks[8];
-  long long fb[3];
-  int fb_rounds;
-#endif
 };
 
 // Block-wide search of t.hist[0, 2048) (bins past the pass's bin count are
@@ -204,7 +186,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int nw = nt >> 5;
   const int n16 = n & ~15;  // keys in whole 16-key runs; the tail is read one by one
-  SPG_TK_MARK(t, 0);
   if (n <= nt) {
     // Few keys: thread i ranks key i by counting the keys that come before it
     // in the total order (key descending, index ascending); the ranks are a
@@ -231,7 +212,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     const int pos = block_exclusive_scan(chosen ? 1 : 0, t.wa, &t.total);
     if (chosen) dst[pos] = base + tid;
     __syncthreads();
-    SPG_TK_MARK(t, 7);
     return;
   }
   if (!minmax_ready) {
@@ -287,7 +267,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
         for (int i = tid; i < 512; i += nt) reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
         __syncthreads();
       }
-      SPG_TK_MARK(t, 1);
       for (int r = tid; r * 16 < n16; r += nt) {
         uint4 v[4];
 #pragma unroll
@@ -308,9 +287,7 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
         if (first || (x & mask) == prefix) atomicAdd(&t.hist[(x >> shift) & (nb - 1)], 1);
       }
       __syncthreads();
-      SPG_TK_MARK(t, 2);
       topk_find_bin(t, need);
-      SPG_TK_MARK(t, 3);
       first = false;
       const int cnt = t.cnt;
       prefix |= static_cast<uint32_t>(t.digit) << shift;
@@ -324,7 +301,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
       hb = shift - 1;
     }
   }
-  SPG_TK_MARK(t, 4);
   // bitmaps of the keys above the bucket / in it: four threads per 32-key
   // word (8 keys each), two words per quad per round, OR-combined with two
   // shuffles
@@ -403,7 +379,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     }
   }
   __syncthreads();
-  SPG_TK_MARK(t, 5);
   if (resolve) {
     // exact threshold among the bucket's keys (cnt <= 256)
     const int cnt = t.ncand;
@@ -435,7 +410,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     need = t.need_thr;
     __syncthreads();
   }
-  SPG_TK_MARK(t, 6);
   // words -> ascending indices, thread j owning words [j*wpt, (j+1)*wpt).
   // Keys equal to the threshold are taken in index order, so the number
   // taken before a thread is min(equal keys before it, need).  One block
@@ -477,7 +451,6 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
     }
   }
   __syncthreads();
-  SPG_TK_MARK(t, 7);
 }
 
 using TopkShared = TopkSmem<8192>;

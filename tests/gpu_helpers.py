@@ -102,9 +102,12 @@ def assert_selection_matches(gpu_sel, scores, P, n_sel, n_sink, n_recent, rel_ga
     assert len(gpu_sel) == len(ref) and fset <= g and gpu_sel == sorted(g)
     for p in cand:
         if float(scores[p]) > sk + band:
-            assert p in g
-        if float(scores[p]) < sk1 - band:
-            assert p not in g
+            assert p in g, f"page {p} scores above the tie band but was not selected"
+    # every selected candidate lies in or above the tie band: a tied page may
+    # stand in for another tied page, never for a lower-scoring one
+    for p in g - fset:
+        assert float(scores[p]) >= sk1 - band, (
+            f"selected page {p} scores {float(scores[p]):.6e}, below the tie band at {sk1 - band:.6e}")
 
 
 def unit_inputs(inp, b, h):

@@ -72,3 +72,46 @@ def test_sketch_step_runs_and_forces_tail():
         assert len(sel) == 6 and sel[-1] == P - 1
         sc = res["scores"][key]
         assert np.isnan(sc[P - 1]) and np.isfinite(sc[: P - 1]).all()
+
+
+@pytest.mark.parametrize("S", [16, 64, 128])
+def test_sketch_metadata_bytes_are_the_stored_arrays(S):
+    """The sketch term counts, per scored block, exactly the bytes the index
+    key occupies: the packed int4 codes of its S tokens x d_s channels and
+    one fp32 scale (measured on arrays built by the oracle's own packer)."""
+    from oracle import sketch
+
+    ds = 16
+    packed = sketch.pack_int4(np.zeros((S, ds), np.int8))
+    per_block = packed.nbytes + np.float32(1.0).nbytes
+    small = obytes.step_bytes([S * 10], 1, 1, 128, S, 1, "sketch", 0, 0, sketch_dim=ds)
+    for n in (1, 7, 159):
+        got = obytes.step_bytes([S * 10], 1, 1, 128, S, 1, "sketch", 0, n, sketch_dim=ds) - small
+        assert got == n * per_block
+    if S == 64:
+        # the 10K-token SALS workload: 16 sequences x 8 kv-heads x 159 scored
+        # blocks of 512 + 4 bytes
+        meta = obytes.step_bytes([10240] * 16, 8, 32, 128, 64, 1, "sketch", 0, 16 * 8 * 159,
+                                 sketch_dim=16) - obytes.step_bytes([10240] * 16, 8, 32, 128, 64, 1,
+                                                                    "sketch", 0, 0, sketch_dim=16)
+        assert meta == 10_501_632
+
+
+@pytest.mark.parametrize("name", ["tiny-quest-gqa4-1k", "llama2-7b-mha-32k", "gqa-serving-b8-4k-64k",
+                                  "sals-int8-b16-10k-4x", "sals-int8-b16-10k-6x", "long-scan-b4-128k"])
+def test_bench_byte_model_equals_the_oracle_byte_model(name):
+    """bench.py keeps its own copy of the byte model (it may not import the
+    oracle on its timed path); both must count the same bytes."""
+    import bench
+
+    w = get_workload(name)
+    kvb = 1 if w.kv_dtype == "i8" else 2
+    for sel_tok, cand, sel_pages in [(0, 0, 0), (2048 * w.num_kv_heads, 2046 * w.num_kv_heads, 128),
+                                     (12345, 6789, 321)]:
+        meta, kv, small = bench.step_bytes(w, None, sel_tok, cand, sel_pages)
+        lens = [w.seq_len or w.seq_range[1]] * w.batch
+        ref = obytes.step_bytes(lens, w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size, kvb,
+                                w.selector, sel_tok, cand, sketch_dim=w.sketch_dim,
+                                scale_bytes=2 if w.kv_dtype == "i8" else 0, q_bytes=2,
+                                sel_pages=sel_pages)
+        assert meta + kv + small == ref

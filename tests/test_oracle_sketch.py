@@ -147,3 +147,62 @@ def test_planted_mistake_is_caught(rng, monkeypatch):
     monkeypatch.setattr(sketch, "quantise_block_int4", truncating)
     with pytest.raises(AssertionError):
         test_quantisation_error_bound(rng)
+
+
+def test_dequant_golden():
+    """Hand-worked int8 code x fp16 scale products (exact in fp32)."""
+    g = json.load(open(os.path.join(GOLDEN, "int8_dequant.json")))
+    for c in g["cases"]:
+        assert float(np.float16(c["scale"])) == c["scale"], "the fixture's scales are fp16 values"
+        got = sketch.dequant(np.array([[c["code"]]], np.int8), np.array([c["scale"]], np.float16))
+        assert got.dtype == np.float32 and float(got[0, 0]) == c["value"]
+
+
+def test_dequant_is_the_exact_product(rng):
+    """Every int8 x fp16 product fits fp32: dequant equals the exact rational product,
+    row by row with each row's own scale (a transposed scale would fail)."""
+    from fractions import Fraction
+
+    codes = rng.integers(-128, 128, (6, 9)).astype(np.int8)
+    scales = (rng.standard_normal(6) * 0.05).astype(np.float16)
+    got = sketch.dequant(codes, scales)
+    for t in range(6):
+        for i in range(9):
+            assert Fraction(float(got[t, i])) == Fraction(int(codes[t, i])) * Fraction(float(scales[t]))
+
+
+def _sketch_unit(rng, S=64, n_blocks=4, d=32):
+    from oracle import decode
+
+    P = n_blocks
+    k = rng.integers(-127, 128, (P, 1, S, d)).astype(np.int8)
+    v = rng.integers(-127, 128, (P, 1, S, d)).astype(np.int8)
+    ks = (rng.random((P, 1, S)) * 0.02 + 0.001).astype(np.float16)
+    vs = (rng.random((P, 1, S)) * 0.02 + 0.001).astype(np.float16)
+    proj = (rng.standard_normal((d, 16)) / 4.0).astype(np.float32)
+    q = rng.standard_normal((1, 2, d)).astype(np.float16)
+    inp = decode.StepInputs(q, k, v, ks, vs, np.arange(P)[None, :], np.array([P * S]), proj)
+    prm = decode.StepParams(S, 3, 0, 1, "sketch", d)
+    return decode, inp, prm
+
+
+def test_sketch_scores_read_the_key_scales_not_the_value_scales(rng):
+    """The index key is built from the dequantised KEYS: new value scales
+    leave every block score unchanged; doubling the key scales (exact in
+    fp16) keeps the int4 codes, doubles each block's sketch scale, and so
+    changes the scores."""
+    decode, inp, prm = _sketch_unit(rng)
+    base = decode.unit_sketch_scores(inp, prm, 0, 0)
+    inp2 = decode.StepInputs(inp.q, inp.k_pool, inp.v_pool, inp.k_scale,
+                             (inp.v_scale.astype(np.float32) * 3.0 + 0.5).astype(np.float16),
+                             inp.page_table, inp.seq_lens, inp.proj)
+    assert np.array_equal(decode.unit_sketch_scores(inp2, prm, 0, 0), base, equal_nan=True)
+    inp3 = decode.StepInputs(inp.q, inp.k_pool, inp.v_pool, (inp.k_scale.astype(np.float32) * 2).astype(np.float16),
+                             inp.v_scale, inp.page_table, inp.seq_lens, inp.proj)
+    c1, s1 = decode.unit_sketch_blocks(inp, prm, 0, 0, [0, 1, 2])
+    c2, s2 = decode.unit_sketch_blocks(inp3, prm, 0, 0, [0, 1, 2])
+    for a, b in zip(c1, c2):
+        assert np.array_equal(a, b)
+    assert [2 * float(x) for x in s1] == [float(x) for x in s2]
+    got = decode.unit_sketch_scores(inp3, prm, 0, 0)
+    assert not np.allclose(got[:-1], base[:-1])
