@@ -42,9 +42,10 @@ NOMINAL_HBM_GBS = 8000.0
 # csrc_sha256; profiles/k_fused_<workload>.md).  Reported only while the code
 # matches.
 NCU_TRAFFIC = {
-    "llama2-7b-mha-32k": (67_790_848, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a"),
-    "long-scan-b4-128k": (205_888_768, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a"),
-    "sals-int8-b16-10k-4x": (100_546_816, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a"),
+    # workload: (DRAM bytes of one launch, code hash, kernel)
+    "llama2-7b-mha-32k": (67_790_848, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a", "k_fused"),
+    "long-scan-b4-128k": (205_888_768, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a", "k_fused"),
+    "sals-int8-b16-10k-4x": (100_546_816, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a", "k_fused"),
 }
 
 
@@ -69,13 +70,13 @@ def csrc_sha256(d: str | None = None) -> str:
     return h.hexdigest()
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, kernel: str = "k_fused"):
     rec = NCU_TRAFFIC.get(workload)
-    if rec is None:
-        return None, "no ncu capture of this workload"
+    if rec is None or rec[2] != kernel:
+        return None, f"no ncu capture of {kernel} on this workload"
     if rec[1] != csrc_sha256():
         return None, "kernel sources changed since the ncu capture"
-    return rec[0], f"profiles/k_fused_{workload}.md"
+    return rec[0], f"profiles/{kernel}_{workload}.md"
 
 
 def dist_env():
@@ -199,15 +200,12 @@ def max_over_ranks(value: float, world: int, device) -> float:
     return float(t.item())
 
 
-def run_ours(args, world, rank, local):
-    import torch.distributed as dist
+PER_WORKLOADS = ["long-scan-b4-128k", "gqa-serving-b8-4k-64k", "sals-int8-b16-10k-4x",
+                 "sals-int8-b16-10k-6x", "llama2-7b-mha-32k"]
 
-    import query_aware_sparse_page_gb300 as spg
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = get_workload(args.workload)
-    R = args.layers
+def build_layers(spg, w, R, dev, rank):
+    """R independent cache replicas ("layers") of workload w, metadata built."""
     layers = []
     for layer in range(R):
         inp = make_inputs(w, device=dev, seed_offset=1000 * rank + layer)
@@ -217,30 +215,22 @@ def run_ours(args, world, rank, local):
                                     bufs.minmax, bufs.sketch, bufs.sketch_scale, inp.proj, bufs.ws)
         layers.append((inp, p, bufs))
     torch.cuda.synchronize()
+    return layers
 
-    # the entry points of one step, per layer
+
+def entry_points(spg, layers):
+    """The entry points of one step, each as a function of the layer index."""
+
     def op_meta(l):
         inp, p, b = layers[l]
         spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 0,
                                     b.minmax, b.sketch, b.sketch_scale, inp.proj, b.ws)
-
-    def op_select_attend(l):
-        inp, p, b = layers[l]
-        spg.sparse_decode_select_attend(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
-                                        inp.page_table, inp.seq_lens, b.minmax, b.sketch,
-                                        b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.out, b.lse,
-                                        b.ws)
 
     def op_step(l):  # the whole hot path, one call
         inp, p, b = layers[l]
         spg.sparse_decode_step(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
                                inp.page_table, inp.seq_lens, b.minmax, b.sketch, b.sketch_scale,
                                inp.proj, b.sel, b.sel_cnt, b.out, b.lse, b.ws)
-
-    def op_separate(l):  # the same step through the separate entry points
-        op_meta(l)
-        op_select(l)
-        op_attn(l)
 
     def op_score(l):
         inp, p, b = layers[l]
@@ -258,26 +248,50 @@ def run_ours(args, world, rank, local):
                                     inp.page_table, inp.seq_lens, b.sel, b.sel_cnt, b.out, b.lse,
                                     b.ws)
 
+    def op_separate(l):  # the same step through the separate entry points
+        op_meta(l)
+        op_select(l)
+        op_attn(l)
+
     def op_dense(l):
         inp, p, b = layers[l]
         spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
                                    inp.page_table, inp.seq_lens, b.out, b.lse, b.ws)
 
-    ops = {"step": op_step, "separate": op_separate, "meta": op_meta, "score": op_score,
-           "select": op_select, "attn": op_attn, "dense": op_dense}
-    for l in range(R):  # eager warm-up of every entry point (kernel attributes, caches)
-        for f in ops.values():
-            f(l)
-    op_step(0)  # leave layer 0 with the step's own selection
-    torch.cuda.synchronize()
+    return {"step": op_step, "separate": op_separate, "meta": op_meta, "score": op_score,
+            "select": op_select, "attn": op_attn, "dense": op_dense}
 
-    K, W = args.steps, args.warmup
 
-    # Each entry point is captured as one CUDA graph over the R layer
-    # replicas in order (a decode pass over R layers, as an engine replays
-    # it), plus a graph of the first K % R layers so that exactly K steps are
-    # timed.  The step is also captured as one graph per layer, to report the
-    # per-launch overhead of replaying single steps.
+class Timer:
+    """CUDA-event timing of K steps on the launching stream, bracketed by a
+    barrier and a device synchronise; max over ranks."""
+
+    def __init__(self, stream, world, dev):
+        self.stream, self.world, self.dev = stream, world, dev
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    def region(self, fn, K):
+        self.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        fn(K)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        self.barrier()
+        return max_over_ranks(e0.elapsed_time(e1), self.world, self.dev) / K
+
+
+def graph_runner(ops, names, R, K):
+    """Each entry point captured as one CUDA graph over the R layer replicas
+    in order (a decode pass over R layers, as an engine replays it), plus a
+    graph of the first K % R layers, so that exactly K steps run."""
+
     def capture(f, layer_ids):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -285,83 +299,159 @@ def run_ours(args, world, rank, local):
                 f(l)
         return g
 
-    graphs = {name: (capture(f, range(R)), capture(f, range(K % R)) if K % R else None)
-              for name, f in ops.items()}
-    single = [capture(op_step, [l]) for l in range(R)]
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream(dev)
+    graphs = {name: (capture(ops[name], range(R)), capture(ops[name], range(K % R)) if K % R else None)
+              for name in names}
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def timed(fn, K):
-        barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K):
-            fn(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        return max_over_ranks(e0.elapsed_time(e1), world, dev) / K
-
-    def timed_graph(name, K):
-        # K steps: K // R replays of the R-layer graph, then the K % R graph
+    def run(name):
         full, part = graphs[name]
-        barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K // R):
-            full.replay()
-        if part is not None:
-            part.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        return max_over_ranks(e0.elapsed_time(e1), world, dev) / K
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    for i in range(-(-W // R)):  # at least W warm-up steps
-        graphs["step"][0].replay()
-    t_end = time.perf_counter() + args.soak
-    while time.perf_counter() < t_end:  # keep the GPU loaded while clocks are sampled
-        graphs["step"][0].replay()
-    ms_step = timed_graph("step", K)
-    clock_info = clocks.stop()
-    clock_info["window"] = "warm-up, soak and timed steps"
+        def go(K_):
+            for _ in range(K_ // R):
+                full.replay()
+            if part is not None:
+                part.replay()
 
-    # per-entry-point durations (K steps each, layers rotating)
-    ms = {name: timed_graph(name, K)
-          for name in ("separate", "meta", "score", "select", "attn", "dense")}
-    ms_single = timed(lambda i: single[i % R].replay(), K)
-    ms_topk = max(ms["select"] - ms["score"], 0.0)
-    # the same step issued eagerly through the Python binding (host-issue bound)
-    ms_eager = timed(lambda i: op_step(i % R), max(K // 4, 10))
+        return go
 
-    # bytes
+    return graphs, run
+
+
+def layer_bytes(w, layers):
+    """Algorithmic bytes of one step (layer 0's selection), and of the dense read."""
     inp0, p0, b0 = layers[0]
     sel_tok, cand, sel_pages = selection_stats(w, inp0, b0.sel, b0.sel_cnt)
     meta_b, kv_b, small_b = step_bytes(w, None, sel_tok, cand, sel_pages)
-    total_b = meta_b + kv_b + small_b
     lens = inp0.seq_lens.cpu().tolist()
-    dense_tok = sum(lens) * w.num_kv_heads
     kvb = 1 if w.kv_dtype == "i8" else 2
-    dense_b = dense_tok * 2 * (w.head_dim * kvb + (2 if w.kv_dtype == "i8" else 0)) + small_b
+    dense_b = sum(lens) * w.num_kv_heads * 2 * (w.head_dim * kvb + (2 if w.kv_dtype == "i8" else 0)) + small_b
+    return meta_b, kv_b, small_b, dense_b
+
+
+def median_spread(xs):
+    return statistics.median(xs), min(xs), max(xs)
+
+
+def measure_workload(spg, name, args, timer, rank, dev):
+    """Step (repeated timed regions), single-step replays and the dense
+    baseline on one workload; a smaller record than the headline's."""
+    w = get_workload(name)
+    R, K = args.layers, args.steps
+    layers = build_layers(spg, w, R, dev, rank)
+    ops = entry_points(spg, layers)
+    for l in range(R):
+        ops["step"](l)
+        ops["dense"](l)
+    ops["step"](0)
+    torch.cuda.synchronize()
+    graphs, run = graph_runner(ops, ["step", "dense"], R, K)
+    single = [torch.cuda.CUDAGraph() for _ in range(R)]
+    for l, g in enumerate(single):
+        with torch.cuda.graph(g):
+            ops["step"](l)
+    for _ in range(max(3, -(-args.warmup // R))):
+        run("step")(R)
+    reps = [timer.region(run("step"), K) for _ in range(args.repeats)]
+    ms_dense = timer.region(run("dense"), K)
+    ms_single = timer.region(lambda K_: [single[i % R].replay() for i in range(K_)], K)
+    ms, lo, hi = median_spread(reps)
+    meta_b, kv_b, small_b, dense_b = layer_bytes(w, layers)
+    total = meta_b + kv_b + small_b
+    peak, _ = measured_peaks()
+    res = {
+        "ms_per_step": round(ms, 5), "ms_min": round(lo, 5), "ms_max": round(hi, 5),
+        "repeats": args.repeats, "steps_per_repeat": K,
+        "steps_per_s": round(1000.0 / ms, 2),
+        "bytes_per_step": total,
+        "hbm_gbs": round(total / (ms * 1e-3) / 1e9, 1),
+        "frac_measured": round(total / (ms * 1e-3) / 1e9 / peak, 4),
+        "single_step_ms": round(ms_single, 5),
+        "single_step_frac_measured": round(total / (ms_single * 1e-3) / 1e9 / peak, 4),
+        "dense_ms": round(ms_dense, 5),
+        "dense_hbm_gbs": round(dense_b / (ms_dense * 1e-3) / 1e9, 1),
+        "speedup_vs_dense": round(ms_dense / ms, 3),
+        "kernel": spg.step_kernel_name(layers[0][1]),
+    }
+    del graphs, single, ops, layers
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, world, rank, local):
+    import query_aware_sparse_page_gb300 as spg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = get_workload(args.workload)
+    R, K, W = args.layers, args.steps, args.warmup
+    layers = build_layers(spg, w, R, dev, rank)
+    ops = entry_points(spg, layers)
+    for l in range(R):  # eager warm-up of every entry point (kernel attributes, caches)
+        for f in ops.values():
+            f(l)
+    ops["step"](0)  # leave layer 0 with the step's own selection
+    torch.cuda.synchronize()
+
+    graphs, run = graph_runner(ops, list(ops), R, K)
+    # the step also as one graph per layer: a step replayed alone, the rate a
+    # model sees when each layer's query depends on the previous layer's output
+    single = []
+    for l in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ops["step"](l)
+        single.append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    timer = Timer(stream, world, dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(max(3, -(-W // R))):  # at least W warm-up steps
+        run("step")(R)
+    t_end = time.perf_counter() + args.soak
+    while time.perf_counter() < t_end:  # keep the GPU loaded while clocks are sampled
+        run("step")(R)
+    reps = [timer.region(run("step"), K) for _ in range(args.repeats)]
+    clock_info = clocks.stop()
+    clock_info["window"] = "warm-up, soak and timed steps"
+    ms_step, ms_lo, ms_hi = median_spread(reps)
+
+    # per-entry-point durations (K steps each, layers rotating)
+    ms = {name: timer.region(run(name), K)
+          for name in ("separate", "meta", "score", "select", "attn", "dense")}
+    ms_single = timer.region(lambda K_: [single[i % R].replay() for i in range(K_)], K)
+    ms_topk = max(ms["select"] - ms["score"], 0.0)
+    # the same step issued eagerly through the Python binding (host-issue bound)
+    ms_eager = timer.region(lambda K_: [ops["step"](i % R) for i in range(K_)], max(K // 4, 10))
+
+    meta_b, kv_b, small_b, dense_b = layer_bytes(w, layers)
+    total_b = meta_b + kv_b + small_b
     peak, peak_kind = measured_peaks()
-
-    # roofline of the dominant kernel: the step is one launch of the fused
-    # kernel (k_fused), timed on its own as the whole step
+    # the other single-launch step kernel on the same replicas (the library
+    # picks the faster one by default; both compute the same step)
+    alt = {}
+    p0 = layers[0][1]
+    default_kernel = spg.step_kernel_name(p0)
+    for code in (spg.STEP_KERNEL_CLUSTER, spg.STEP_KERNEL_SCHED):
+        spg.spg_set_step_kernel(code)
+        name = spg.step_kernel_name(p0)
+        if name == default_kernel or name is None:
+            continue
+        g_alt, run_alt = graph_runner(ops, ["step"], R, K)
+        run_alt("step")(R)
+        ms_alt = statistics.median(timer.region(run_alt("step"), K) for _ in range(3))
+        alt[name] = {"ms_per_step": round(ms_alt, 5), "steps_per_s": round(1000.0 / ms_alt, 2),
+                     "frac_measured": round(total_b / (ms_alt * 1e-3) / 1e9 / peak, 4)}
+        del g_alt
+    spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
     score_name = "k_quest_select" if w.selector == "quest" else "k_sketch_select"
-    kname, dom_ms, dom_bytes = "k_fused", ms_step, total_b
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else 0.0
-
-    traffic, traffic_src = ncu_traffic(w.name)
+    # the step is one launch of the persistent kernel, timed as the whole step
+    kname = spg.step_kernel_name(layers[0][1])
+    achieved = total_b / (ms_step * 1e-3) / 1e9 if ms_step > 0 else 0.0
+    traffic, traffic_src = ncu_traffic(w.name, kname)
     e2e = run_e2e(args, spg, layers, stream, world, dev)
-    launches_per_step = 1 if (w.selector == "quest" and w.max_pages_per_seq <= 8192) else 2
+    launches_per_step = spg.step_launch_count(layers[0][1])
 
     steps_s = world * 1000.0 / ms_step
     gbs = world * total_b / (ms_step * 1e-3) / 1e9
@@ -388,8 +478,12 @@ def run_ours(args, world, rank, local):
             "l2": f"inputs larger than L2: {R} rotating cache replicas, each step reads "
                   f"{total_b / 1e6:.1f} MB of a distinct replica",
             "launch": f"CUDA graph of sparse_decode_step over the {R} layer replicas in order",
+            "timing": f"median of {args.repeats} timed regions of exactly {K} steps each",
             "parallelism": "replicas" if world > 1 else "single",
         },
+        "repeats_ms_per_step": [round(x, 5) for x in reps],
+        "ms_per_step_min": round(ms_lo, 5),
+        "ms_per_step_max": round(ms_hi, 5),
         "hbm_gbs_effective": round(gbs, 1),
         "hbm_frac_nominal": round(gbs / world / NOMINAL_HBM_GBS, 4),
         "hbm_frac_measured": round(gbs / world / peak, 4),
@@ -409,6 +503,8 @@ def run_ours(args, world, rank, local):
         },
         "eager_steps_per_s": round(world * 1000.0 / ms_eager, 2),
         "graph_per_step_steps_per_s": round(world * 1000.0 / ms_single, 2),
+        "graph_per_step_frac_measured": round(total_b / (ms_single * 1e-3) / 1e9 / peak, 4),
+        "other_step_kernels": alt,
         "roofline": {
             "kernel": kname,
             "bound": "hbm",
@@ -419,15 +515,23 @@ def run_ours(args, world, rank, local):
             "peak_kind": peak_kind,
             "traffic": traffic,
             "traffic_source": traffic_src,
-            "algorithmic_bytes": dom_bytes,
-            "ms_per_launch": round(float(dom_ms), 5),
+            "algorithmic_bytes": total_b,
+            "ms_per_launch": round(float(ms_step), 5),
         },
         "clocks": clock_info,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
     }
+    del graphs, single, ops
+    if not args.no_per_workload:
+        layers = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        res["per_workload"] = {n: measure_workload(spg, n, args, timer, rank, dev)
+                               for n in PER_WORKLOADS if n != w.name}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, layers[0][0], budget_s=args.cpu_seconds)
+        inp0 = make_inputs(w, device=dev, seed_offset=1000 * rank)
+        res["cpu_baseline"] = cpu_baseline(w, inp0, budget_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(res), flush=True)
 
@@ -508,10 +612,11 @@ def _oracle_unit_inputs(inp, b, h):
                              np.arange(max(P, 1))[None, :], np.array([L]), proj)
 
 
-def cpu_baseline(w, inp, budget_s=12.0, max_units=None):
+def cpu_baseline_single(w, inp, budget_s=12.0, max_units=None):
     """Time the oracle, as it stands, on whole steps (every (batch, kv-head)
-    unit) of this workload, repeated until about `budget_s` seconds of CPU
-    work are spent; `cores` is the process CPU time over the wall time."""
+    unit) of this workload in this process, repeated until about `budget_s`
+    seconds of CPU work are spent; `cores` is the process CPU time over the
+    wall time."""
     from oracle import decode
 
     prm = decode.StepParams(w.page_size, w.n_sel_pages, w.n_sink, w.n_recent, w.selector, w.head_dim)
@@ -534,7 +639,63 @@ def cpu_baseline(w, inp, budget_s=12.0, max_units=None):
     return {"value": round(steps / wall, 6), "unit": "steps/s", "cores": cores, "kind": "oracle",
             "sample": f"{done} (batch, kv-head) units = {steps:.2f} steps of {w.name} "
                       f"({len(units)} units per step), {wall:.1f} s wall / {cpu:.1f} s CPU of "
-                      f"fp64 numpy on the host"}
+                      f"fp64 numpy in one process"}
+
+
+def cpu_baseline_parallel(w, inp, budget_s=12.0):
+    """The oracle on every host core at once: one process per core (started
+    with python -m oracle.run_units, no torch in them, one BLAS thread each),
+    each running its share of the step's (batch, kv-head) units round-robin
+    for `budget_s` seconds; steps/s = the sum of the processes' unit rates
+    over the units of a step."""
+    import tempfile
+
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    n_cores = os.cpu_count() or 1
+    n_proc = max(1, min(n_cores, len(units)))
+    sel_id = {"quest": 0, "sketch": 1, "all": 2}[w.selector]
+    arrays = {"params": np.array([w.page_size, w.n_sel_pages, w.n_sink, w.n_recent, w.head_dim,
+                                  sel_id, len(units)], dtype=np.int64)}
+    for i, (b, h) in enumerate(units):
+        sub = _oracle_unit_inputs(inp, b, h)
+        for k, v in (("q", sub.q), ("k", sub.k_pool), ("v", sub.v_pool), ("ks", sub.k_scale),
+                     ("vs", sub.v_scale), ("pt", sub.page_table), ("lens", sub.seq_lens),
+                     ("proj", sub.proj)):
+            if v is not None:
+                arrays[f"u{i}_{k}"] = v
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "units.npz")
+        np.savez(path, **arrays)
+        procs = [subprocess.Popen([sys.executable, "-m", "oracle.run_units", path, str(i), str(n_proc),
+                                   str(budget_s)], cwd=ROOT, env=env, stdout=subprocess.PIPE,
+                                  stderr=subprocess.PIPE, text=True)
+                 for i in range(n_proc)]
+        outs = [p.communicate(timeout=budget_s + 300) for p in procs]
+    recs = []
+    for (o, e), p in zip(outs, procs):
+        if p.returncode != 0:
+            return {"error": f"oracle worker failed: {e.strip()[-300:]}"}
+        recs.append(json.loads(o.strip().splitlines()[-1]))
+    unit_rate = sum(r["units"] / r["wall"] for r in recs if r["wall"] > 0)
+    done = sum(r["units"] for r in recs)
+    cpu = sum(r["cpu"] for r in recs)
+    return {"value": round(unit_rate / len(units), 6), "unit": "steps/s", "cores": n_proc,
+            "kind": "oracle", "host_cores": n_cores,
+            "sample": f"{done} (batch, kv-head) units of {w.name} ({len(units)} per step) on "
+                      f"{n_proc} processes x {budget_s:.0f} s, {cpu:.0f} s CPU in all, fp64 numpy"}
+
+
+def cpu_baseline(w, inp, budget_s=12.0):
+    """Both oracle timings; the headline is the one on every host core."""
+    single = cpu_baseline_single(w, inp, budget_s=budget_s / 2)
+    par = cpu_baseline_parallel(w, inp, budget_s=budget_s / 2)
+    if "error" in par:
+        single["parallel"] = par
+        single["host_cores"] = os.cpu_count() or 1
+        return single
+    par["single_process"] = single
+    return par
 
 
 def run_reference(args, world, rank, local):
@@ -618,6 +779,8 @@ def main():
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions of K steps (median reported)")
+    ap.add_argument("--no-per-workload", action="store_true", help="only the headline workload")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if world > 1:

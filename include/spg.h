@@ -32,7 +32,10 @@
  *     skipped and a bit (SPG_DEVERR_*) is OR-ed into the error word at the
  *     start of the workspace.  spg_read_device_error() fetches it.
  *   - The workspace must be zero-filled once after allocation; the library
- *     leaves its bookkeeping in a reusable state after every call.
+ *     leaves its bookkeeping in a reusable state after every call.  After a
+ *     call that reported SPG_DEVERR_TIMEOUT, zero it again before reuse.
+ *     Calls that share a workspace must not overlap on the GPU (order them
+ *     on one stream).
  *
  * Shapes (B batch, Hq / Hkv query / kv heads, G = Hq / Hkv, d head_dim,
  * S page_size, P_phys num_phys_pages, MP max_pages_per_seq,
@@ -111,7 +114,10 @@ typedef struct spg_params {
   int32_t num_q_heads;       /* Hq, a multiple of num_kv_heads, G = Hq/Hkv in {1,2,4,8} */
   int32_t num_kv_heads;      /* Hkv >= 1 */
   int32_t head_dim;          /* d in {64, 128} */
-  int32_t page_size;         /* S: 8, 16, 32, 64 or 128 tokens (a SALS block) */
+  int32_t page_size;         /* S: 16, 32, 64 or 128 tokens (a SALS block); 8 is
+                                valid but not built (SPG_EUNSUPPORTED), and so is a
+                                page whose K + V (+ int8 scales) of one kv-head
+                                exceed 34 KB (fp16/bf16 at d = 128: S <= 64) */
   int32_t num_phys_pages;    /* P_phys: pages in the pool */
   int32_t max_pages_per_seq; /* MP: columns of page_table */
   int32_t kv_dtype;          /* spg_dtype */
@@ -178,6 +184,26 @@ spg_status sparse_page_select(const spg_params* p, const void* q, const int32_t*
                               const float* sketch_scale, const float* proj, int32_t* sel,
                               int32_t* sel_cnt, void* ws, size_t ws_bytes, spg_stream_t stream);
 
+/* The sketch selector's integer arithmetic, for checking it exactly (SALS
+ * 长序列推理优化, Quant Sals Indexer steps 1-2: the int4 index key times the
+ * int8 index query as an integer matrix product, before any dequantisation).
+ * Per (batch, kv-head) unit, with the same device routines the decode step's
+ * scan uses:
+ *   qc   [B][Hkv][16] int32  the int8 index-query codes (group-mean query
+ *                            projected through proj, scale max|q~|/127,
+ *                            round half to even), one code per int32
+ *   sq   [B][Hkv] fp32       the index-query scale
+ *   dots [B][Hkv][MP][S] int32  for every token t of every candidate block
+ *                            p in [n_sink, P_b - n_recent): sum_j qc_j *
+ *                            code_{p,t,j}, exact; every other entry is 0
+ * Sketch selector only (SPG_EINVAL otherwise); sketch holds the int4 codes
+ * of sparse_page_meta_update.  Device-detected faults go to the workspace
+ * error word. */
+spg_status sparse_page_sketch_dots(const spg_params* p, const void* q, const int32_t* seq_lens,
+                                   const uint8_t* sketch, const float* proj, int32_t* qc,
+                                   float* sq, int32_t* dots, void* ws, size_t ws_bytes,
+                                   spg_stream_t stream);
+
 /* Flash-decoding over the selected pages only (SALS SFAA; Quest
  * Approximate attention): for query head j of kv-head h, attention over
  * the tokens t < seq_lens[b] of pages sel[b][h][0..sel_cnt), softmax
@@ -205,7 +231,8 @@ spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const
  * appended at seq_lens[b]-1 (as sparse_page_meta_update with rebuild == 0),
  * then sparse_decode_select_attend.  Where the parameters allow it (page
  * tables of at most 8192 pages), selection and attention run as one launch
- * of one 8-CTA thread-block cluster per (batch, kv-head); with
+ * of one 8-CTA thread-block cluster per (batch, kv-head), or as one
+ * persistent launch with task queues (spg_step_kernel says which); with
  * n_recent_pages >= 1 (and sketch_dim 16 for the sketch selector) the append
  * runs inside that launch too (the appended token's page is forced, so no
  * scoring depends on it). */
@@ -256,6 +283,25 @@ spg_status sparse_decode_attention_noalloc(const spg_params* p, const void* q, c
                                            const int32_t* seq_lens, const int32_t* sel,
                                            const int32_t* sel_cnt, float* out, float* lse,
                                            spg_stream_t stream);
+
+/* Which kernel(s) sparse_decode_step launches for these parameters (host
+ * only; NULL when spg_validate rejects them): "k_fused" (one thread-block
+ * cluster per unit), "k_sched" (the persistent scheduled step), or the
+ * separate scoring and attention kernels.  A diagnostic for benchmarks and
+ * tests; the choice is made by the library (see spg_set_step_kernel). */
+const char* spg_step_kernel(const spg_params* p);
+
+/* Kernel launches one sparse_decode_step call makes for these parameters
+ * (host only; 0 when spg_validate rejects them). */
+int32_t spg_step_launches(const spg_params* p);
+
+/* Process-wide preference between the two single-launch step kernels, for
+ * comparing them: 0 = automatic (the cluster kernel where it applies, else
+ * the scheduled kernel), 1 = the cluster kernel only, 2 = the scheduled
+ * kernel only (shapes it does not take use the separate kernels).  Results are the
+ * same up to the order of floating-point sums.  Not thread-safe with respect
+ * to launches in flight on other host threads.  SPG_EINVAL for other values. */
+spg_status spg_set_step_kernel(int32_t kernel);
 
 /* Waits for `stream`, then copies the workspace error word to *bits. */
 spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t stream);

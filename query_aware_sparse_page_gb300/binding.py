@@ -90,6 +90,10 @@ def _load():
         "dense_decode_attention": ([P, v, v, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
         "sparse_decode_step": (
             [P, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
+        "sparse_page_sketch_dots": ([P, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
+        "spg_step_kernel": ([P], c_char_p),
+        "spg_step_launches": ([P], c_int32),
+        "spg_set_step_kernel": ([c_int32], c_int32),
         "spg_read_device_error": ([v, POINTER(c_int32), v], c_int32),
         "spg_clear_device_error": ([v, v], c_int32),
     }
@@ -153,6 +157,27 @@ def spg_workspace_size(p: spg_params) -> int:
     return n.value
 
 
+def spg_step_kernel(p: spg_params) -> str | None:
+    r = LIB.spg_step_kernel(ctypes.byref(p))
+    return None if r is None else r.decode()
+
+
+step_kernel_name = spg_step_kernel
+
+
+def spg_step_launches(p: spg_params) -> int:
+    return LIB.spg_step_launches(ctypes.byref(p))
+
+
+step_launch_count = spg_step_launches
+
+STEP_KERNEL_AUTO, STEP_KERNEL_CLUSTER, STEP_KERNEL_SCHED = 0, 1, 2
+
+
+def spg_set_step_kernel(kernel: int):
+    _check(LIB.spg_set_step_kernel(int(kernel)), "spg_set_step_kernel")
+
+
 # ---- device entry points -------------------------------------------------------
 def sparse_page_meta_update(p, k_pool, k_scale, page_table, seq_lens, rebuild, minmax=None,
                             sketch=None, sketch_scale=None, proj=None, ws=None, stream=None):
@@ -170,6 +195,13 @@ def sparse_page_score(p, q, page_table, seq_lens, minmax=None, sketch=None, sket
         ctypes.byref(p), _ptr(q), _ptr(page_table), _ptr(seq_lens), _ptr(minmax), _ptr(sketch),
         _ptr(sketch_scale), _ptr(proj), _ptr(scores), wp, wn, _stream(stream)),
         "sparse_page_score")
+
+
+def sparse_page_sketch_dots(p, q, seq_lens, sketch, proj, qc, sq, dots, ws, stream=None):
+    wp, wn = _ws(ws)
+    _check(LIB.sparse_page_sketch_dots(
+        ctypes.byref(p), _ptr(q), _ptr(seq_lens), _ptr(sketch), _ptr(proj), _ptr(qc), _ptr(sq),
+        _ptr(dots), wp, wn, _stream(stream)), "sparse_page_sketch_dots")
 
 
 def sparse_page_select(p, q, page_table, seq_lens, minmax=None, sketch=None, sketch_scale=None,

@@ -1,5 +1,7 @@
 // C ABI of libspg: parameter validation, workspace layout, launch sequencing.
 // Everything here runs on the host; all device work is in the kernel files.
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -25,25 +27,40 @@ int device_sm_count() {
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace layout (every region 256-byte aligned):
+//   header    256 B: error word at 0, the scheduled step's queue counters at 64
+//   counters  [B*Hkv] int32: split arrivals of the attention kernel
+//   sel_cnt.  [B*Hkv] int32: scoring CTAs done, for the fused selection
+//   scores    [B*Hkv][MP] fp32 (the scheduled step keeps its keys here)
+//   pm, pl    [B*Hq][kMaxSplits] fp32; pacc [B*Hq][kMaxSplits][d] fp32
+//   flags     [4][B*Hkv] int32 (scheduled step)
+//   slices    [B*Hkv][n_sel] int2 (scheduled step)
+//   iq        [B*Hkv][8] int32 (scheduled step, sketch selector)
 size_t workspace_bytes(const spg_params& p) {
   const size_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
   const size_t d = p.head_dim, MP = p.max_pages_per_seq;
-  size_t off = 256;                                      // header: error word
+  const size_t n_sel = p.selector == SPG_SEL_ALL ? 1 : std::max(1, n_sel_pages(p));
+  size_t off = 256;                                      // header: error word, queue counters
   off += align256(sizeof(int32_t) * B * Hkv);            // split arrival counters
   off += align256(sizeof(int32_t) * B * Hkv);            // scoring arrival counters
-  off += align256(sizeof(float) * B * Hkv * MP);         // scores
+  off += align256(sizeof(float) * B * Hkv * MP);         // scores / keys
   off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pm
   off += align256(sizeof(float) * B * Hq * kMaxSplits);  // pl
   off += align256(sizeof(float) * B * Hq * kMaxSplits * d);  // pacc
+  off += align256(sizeof(int32_t) * 4 * B * Hkv);        // per-unit flags
+  off += align256(sizeof(int2) * B * Hkv * n_sel);       // selection slices
+  off += align256(sizeof(int32_t) * 8 * B * Hkv);        // index queries
   return off;
 }
 
 Workspace carve_workspace(const spg_params& p, void* ws) {
   const size_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads, d = p.head_dim;
   const size_t MP = p.max_pages_per_seq;
+  const size_t n_sel = p.selector == SPG_SEL_ALL ? 1 : std::max(1, n_sel_pages(p));
   uint8_t* base = static_cast<uint8_t*>(ws);
   Workspace w{};
   w.err = reinterpret_cast<int32_t*>(base);
+  w.sched_ctr = reinterpret_cast<int32_t*>(base + 64);
   size_t off = 256;
   w.counters = reinterpret_cast<int32_t*>(base + off);
   off += align256(sizeof(int32_t) * B * Hkv);
@@ -56,6 +73,12 @@ Workspace carve_workspace(const spg_params& p, void* ws) {
   w.pl = reinterpret_cast<float*>(base + off);
   off += align256(sizeof(float) * B * Hq * kMaxSplits);
   w.pacc = reinterpret_cast<float*>(base + off);
+  off += align256(sizeof(float) * B * Hq * kMaxSplits * d);
+  w.sched_flags = reinterpret_cast<int32_t*>(base + off);
+  off += align256(sizeof(int32_t) * 4 * B * Hkv);
+  w.slices = reinterpret_cast<int2*>(base + off);
+  off += align256(sizeof(int2) * B * Hkv * n_sel);
+  w.iq = reinterpret_cast<int32_t*>(base + off);
   return w;
 }
 
@@ -85,17 +108,36 @@ spg_status check_meta_inputs(const spg_params* p, const void* minmax, const uint
   return SPG_EINVAL;  // SPG_SEL_ALL has no metadata and no selection
 }
 
-// select + attend: one cluster launch when the parameters allow it, else the
-// scoring/selection launch followed by the split-K attention launch.  With
-// append != 0 the fused launch also applies the Quest metadata append.
+// Kernel preference for the single-launch step, process-wide
+// (spg_set_step_kernel): 0 automatic, 1 cluster kernel, 2 scheduled kernel.
+std::atomic<int> g_step_pref{0};
+
+bool use_fused(const spg_params& p, int append) {
+  return g_step_pref.load() != 2 && spg::fused_supported(p, append);
+}
+bool use_sched(const spg_params& p, int append) {
+  return g_step_pref.load() != 1 && spg::sched_supported(p, append);
+}
+
+// select + attend: one cluster launch when the parameters allow it (the
+// faster single-launch kernel on every measured workload), else one
+// persistent scheduled launch, else the scoring/selection launch followed by
+// the split-K attention launch.  With append != 0 the single-launch kernels
+// also apply the metadata append of the new token.
 cudaError_t select_attend(const spg_params& p, const void* q, const void* k_pool,
                           const void* v_pool, const void* k_scale, const void* v_scale,
                           const int32_t* page_table, const int32_t* seq_lens, void* minmax,
                           const uint8_t* sketch, const float* sketch_scale, const float* proj,
                           int32_t* sel, int32_t* sel_cnt, float* out, float* lse, int append,
                           const Workspace& w, cudaStream_t st) {
-  if (spg::fused_supported(p, append)) {
+  if (use_fused(p, append)) {
     const cudaError_t e = spg::launch_fused(p, q, k_pool, v_pool, k_scale, v_scale, page_table,
+                                            seq_lens, minmax, sketch, sketch_scale, proj, sel,
+                                            sel_cnt, out, lse, append, w, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  if (use_sched(p, append)) {
+    const cudaError_t e = spg::launch_sched(p, q, k_pool, v_pool, k_scale, v_scale, page_table,
                                             seq_lens, minmax, sketch, sketch_scale, proj, sel,
                                             sel_cnt, out, lse, append, w, st);
     if (e != cudaErrorNotSupported) return e;
@@ -139,6 +181,9 @@ const char* spg_status_str(int32_t s) {
   }
 }
 
+// largest K + V (+ scales) bytes of one page of one kv-head
+constexpr int64_t kMaxPageBytes = 34 * 1024;
+
 spg_status spg_validate(const spg_params* p) {
   if (!p) return SPG_EINVAL;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1) return SPG_EINVAL;
@@ -167,6 +212,15 @@ spg_status spg_validate(const spg_params* p) {
   if (p->head_dim != 64 && p->head_dim != 128) return SPG_EUNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8) return SPG_EUNSUPPORTED;
   if (p->selector == SPG_SEL_QUEST && p->kv_dtype == SPG_I8) return SPG_EUNSUPPORTED;
+  // the tensor-core consumers take 16-token tiles of a staged page, and a
+  // ring of four stages must hold four pages (K, V and int8 scales)
+  if (p->page_size < 16) return SPG_EUNSUPPORTED;
+  {
+    const int64_t elem = p->kv_dtype == SPG_I8 ? 1 : 2;
+    const int64_t page_bytes = 2 * static_cast<int64_t>(p->page_size) * p->head_dim * elem +
+                               (p->kv_dtype == SPG_I8 ? 4 * p->page_size : 0);
+    if (page_bytes > kMaxPageBytes) return SPG_EUNSUPPORTED;
+  }
   if (p->selector != SPG_SEL_ALL && p->max_pages_per_seq > spg::kMaxTopkPages)
     return SPG_EUNSUPPORTED;
   if (p->max_pages_per_seq > spg::kMaxSplits * 1024) return SPG_EUNSUPPORTED;
@@ -288,7 +342,7 @@ spg_status sparse_decode_step(const spg_params* p, const void* q, const void* k_
   const Workspace w = spg::carve_workspace(*p, ws);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  int append_inside = spg::fused_supported(*p, 1) ? 1 : 0;
+  int append_inside = (use_sched(*p, 1) || use_fused(*p, 1)) ? 1 : 0;
   if (!append_inside)
     e = spg::launch_meta_update(*p, k_pool, k_scale, page_table, seq_lens, 0, minmax, sketch,
                                 sketch_scale, proj, w.err, st);
@@ -313,6 +367,44 @@ spg_status dense_decode_attention(const spg_params* p, const void* q, const void
   return cuda_status(spg::launch_attention(*p, q, k_pool, v_pool, k_scale, v_scale, page_table,
                                            seq_lens, nullptr, nullptr, out, lse, w,
                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spg_status sparse_page_sketch_dots(const spg_params* p, const void* q, const int32_t* seq_lens,
+                                   const uint8_t* sketch, const float* proj, int32_t* qc,
+                                   float* sq, int32_t* dots, void* ws, size_t ws_bytes,
+                                   spg_stream_t stream) {
+  spg_status s = spg_validate(p);
+  if (s != SPG_OK) return s;
+  if (p->selector != SPG_SEL_SKETCH_INT4) return SPG_EINVAL;
+  if (!ok_ptr(q) || !ok_ptr(seq_lens) || !ok_ptr(sketch) || !ok_ptr(proj) || !ok_ptr(qc) ||
+      !ok_ptr(sq) || !ok_ptr(dots))
+    return SPG_EINVAL;
+  if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
+  const Workspace w = spg::carve_workspace(*p, ws);
+  return cuda_status(spg::launch_sketch_dots(*p, q, seq_lens, sketch, proj, qc, sq, dots, w.err,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* spg_step_kernel(const spg_params* p) {
+  if (spg_validate(p) != SPG_OK) return nullptr;
+  if (p->selector == SPG_SEL_ALL) return "k_attn";
+  if (use_fused(*p, 1)) return "k_fused";
+  if (use_sched(*p, 1)) return "k_sched";
+  return p->selector == SPG_SEL_QUEST ? "k_quest_select+k_attn" : "k_sketch_select+k_attn";
+}
+
+int32_t spg_step_launches(const spg_params* p) {
+  if (spg_validate(p) != SPG_OK) return 0;
+  if (p->selector == SPG_SEL_ALL) return 1;
+  if (use_sched(*p, 1) || use_fused(*p, 1)) return 1;
+  // append, scoring (+ a separate selection kernel past 8192 pages), attention
+  return p->max_pages_per_seq > 8192 ? 4 : 3;
+}
+
+spg_status spg_set_step_kernel(int32_t kernel) {
+  if (kernel < 0 || kernel > 2) return SPG_EINVAL;
+  g_step_pref.store(kernel);
+  return SPG_OK;
 }
 
 spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t stream) {

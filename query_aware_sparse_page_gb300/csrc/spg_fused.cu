@@ -43,6 +43,7 @@
 // which every thread of every CTA reaches on every path; all mbarrier waits
 // are bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still
 // reaches the cluster barriers.
+#include "spg_append.cuh"
 #include "spg_attn_core.cuh"
 #include "spg_internal.h"
 #include "spg_select_core.cuh"
@@ -105,36 +106,6 @@ __device__ __forceinline__ void smem_chunk(const uint8_t* p, uint32_t (&w)[CPL /
   }
 }
 
-// Quest append of the token at L-1 for (b, h) by one warp (Quest 完全拆解,
-// 关键性估计算法); the page's first token starts its statistics.
-template <typename T, int D>
-__device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int lane) {
-  constexpr int CPL = D / 32;
-  const int S = a.S, t = L - 1, p = t / S, slot = t % S;
-  const int phys = a.page_table[static_cast<size_t>(b) * a.MP + p];
-  if (phys < 0 || phys >= a.n_phys) {
-    if (lane == 0) record_error(a.err, SPG_DEVERR_PAGE_ID);
-    return;
-  }
-  const size_t ph = static_cast<size_t>(phys) * a.Hkv + h;
-  const T* k = static_cast<const T*>(a.k_pool) + (ph * S + slot) * D + lane * CPL;
-  T* row = static_cast<T*>(a.minmax) + ((static_cast<size_t>(b) * a.Hkv + h) * a.MP + p) * 2 * D;
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const T kv = k[c];
-    T& lo = row[meta_swz<T>(lane * CPL + c, p)];
-    T& hi = row[meta_swz<T>(D + lane * CPL + c, p)];
-    if (slot == 0) {
-      lo = kv;
-      hi = kv;
-    } else {
-      const float kf = to_f32(kv);
-      if (kf < to_f32(lo)) lo = kv;
-      if (kf > to_f32(hi)) hi = kv;
-    }
-  }
-}
-
 // Sketch of the block completed by the token at L-1 (when L is a multiple of
 // S; SALS长序列推理优化, the low-rank index key of a block), split over the
 // auxiliary warps of the cluster's C CTAs: CTA r takes tokens
@@ -149,20 +120,6 @@ __device__ void append_minmax_warp(const FusedArgs& a, int b, int h, int L, int 
 // what is written.
 constexpr int kSketchVals = 16;  // one token's 16 sketch values per lane: S / C <= 32
 
-// 16 consecutive channels of a key row as fp32 (row 16-byte aligned)
-template <typename T>
-__device__ __forceinline__ void load16_f32(const T* p, float (&x)[16]) {
-  if constexpr (sizeof(T) == 1) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] = static_cast<float>(static_cast<int8_t>((ws[e >> 2] >> (8 * (e & 3))) & 0xffu));
-  } else {
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) load_cvt<T, 8>(p + 8 * hf, x + 8 * hf);
-  }
-}
-
 template <typename T, int D>
 __device__ void sketch_append_part1(const FusedArgs& a, int b, int h, int L, int lane, uint32_t rank,
                                     int C, float (&v)[kSketchVals], float* s_samax) {
@@ -176,27 +133,9 @@ __device__ void sketch_append_part1(const FusedArgs& a, int b, int h, int L, int
   if (phys >= 0 && phys < a.n_phys) {
     if (lane < tpc) {
       const size_t ph = static_cast<size_t>(phys) * a.Hkv + h;
-      const T* krow = static_cast<const T*>(a.k_pool) + (ph * S + t) * D;
       float sc = 1.f;
       if constexpr (is_i8<T>()) sc = __half2float(a.k_scale[ph * S + t]);
-      const float4* P4 = reinterpret_cast<const float4*>(a.proj);  // [D][DS] row-major
-      for (int ic = 0; ic < D; ic += 16) {
-        float x[16];
-        load16_f32<T>(krow + ic, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float kv = x[e];
-          if constexpr (is_i8<T>()) kv = __fmul_rn(kv, sc);
-#pragma unroll
-          for (int q4 = 0; q4 < DS / 4; ++q4) {
-            const float4 pv = __ldg(P4 + (ic + e) * (DS / 4) + q4);
-            v[4 * q4] = __fadd_rn(v[4 * q4], __fmul_rn(kv, pv.x));
-            v[4 * q4 + 1] = __fadd_rn(v[4 * q4 + 1], __fmul_rn(kv, pv.y));
-            v[4 * q4 + 2] = __fadd_rn(v[4 * q4 + 2], __fmul_rn(kv, pv.z));
-            v[4 * q4 + 3] = __fadd_rn(v[4 * q4 + 3], __fmul_rn(kv, pv.w));
-          }
-        }
-      }
+      sketch_project_row<T, D>(static_cast<const T*>(a.k_pool) + (ph * S + t) * D, sc, a.proj, v);
 #pragma unroll
       for (int u = 0; u < DS; ++u) amax = fmaxf(amax, fabsf(v[u]));
     }
@@ -366,7 +305,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       mbar_arrive(&s_ptbar);
     }
     if constexpr (SEL == 0) {
-      if (a.append && rank == C - 1 && L > 0) append_minmax_warp<T, D>(a, b, h, L, lane);
+      if (a.append && rank == C - 1 && L > 0)
+        minmax_append_warp<T, D>(static_cast<const T*>(a.k_pool), a.page_table, static_cast<T*>(a.minmax),
+                                 a.err, a.Hkv, a.S, a.MP, a.n_phys, b, h, L, lane);
     } else {
       // the sketch of a block is written when the block fills (every CTA's
       // aux warp takes a slice)
@@ -415,11 +356,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       // index query of the group, built by the consumer warps only
       const TQ* qb = static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D;
       constexpr int DS = 16;
-      for (int i = threadIdx.x; i < D; i += CW * 32) {
-        float s = to_f32(qb[i]);
-        for (int g = 1; g < G; ++g) s = __fadd_rn(s, to_f32(qb[g * D + i]));
-        s_qbar[i] = __fdiv_rn(s, static_cast<float>(G));
-      }
       {  // P (16-byte aligned): all of a thread's loads in flight at once
         constexpr int NV = D * DS / 4 / (CW * 32);
         const float4* P4 = reinterpret_cast<const float4*>(a.proj);
@@ -431,26 +367,13 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       }
       consumers_sync();
       if (warp == 0) {
-        float qt = 0.f;
-        if (lane < DS) {
-          // products in any order, the sum in channel order
-#pragma unroll 16
-          for (int i = 0; i < D; ++i) qt = __fadd_rn(qt, __fmul_rn(s_qbar[i], s_P[i * DS + lane]));
-        }
-        float am = fabsf(qt);
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        const float sq = am > 0.f ? __fdiv_rn(am, 127.0f) : 1.0f;
-        const int qc = max(-127, min(127, static_cast<int>(rintf(__fdiv_rn(qt, sq)))));
-        int c[DS];
-#pragma unroll
-        for (int j = 0; j < DS; ++j) c[j] = __shfl_sync(0xffffffffu, qc, j);
+        int c4[4];
+        float sqv;
+        sketch_index_query_warp<TQ>(qb, G, D, s_P, s_qbar, lane, c4, sqv);
         if (lane == 0) {
-          s_qc[0] = pack_i8x4(c[0], c[2], c[4], c[6]);
-          s_qc[1] = pack_i8x4(c[1], c[3], c[5], c[7]);
-          s_qc[2] = pack_i8x4(c[8], c[10], c[12], c[14]);
-          s_qc[3] = pack_i8x4(c[9], c[11], c[13], c[15]);
-          s_sq = sq;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s_qc[k] = c4[k];
+          s_sq = sqv;
         }
       }
       consumers_sync();

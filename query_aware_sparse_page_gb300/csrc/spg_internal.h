@@ -19,6 +19,11 @@ struct Workspace {
   float* pm;        // [B][Hq][kMaxSplits] running max (log2 domain)
   float* pl;        // [B][Hq][kMaxSplits] running sum
   float* pacc;      // [B][Hq][kMaxSplits][d] unnormalised output
+  // the persistent scheduled step (spg_sched.cu)
+  int32_t* sched_ctr;    // [8] queue counters (in the header); zero between calls
+  int32_t* sched_flags;  // [4][B*Hkv] per-unit flags; zero between calls
+  int2* slices;          // [B*Hkv][n_sel] (physical page, valid tokens) of the selection
+  int32_t* iq;           // [B*Hkv][8] sketch index queries
 };
 
 size_t workspace_bytes(const spg_params& p);
@@ -60,11 +65,27 @@ cudaError_t launch_attention(const spg_params& p, const void* q, const void* k_p
                              const int32_t* sel, const int32_t* sel_cnt, float* out, float* lse,
                              const Workspace& ws, cudaStream_t stream);
 
+// The sketch selector's index query codes / scale and per-token integer
+// dots of every candidate block (sparse_page_sketch_dots).
+cudaError_t launch_sketch_dots(const spg_params& p, const void* q, const int32_t* seq_lens,
+                               const uint8_t* sketch, const float* proj, int32_t* qc, float* sq,
+                               int32_t* dots, int32_t* err, cudaStream_t stream);
+
 // The whole step in one cluster launch (see spg_fused.cu).  fused_supported
 // says whether these parameters can take that path; launch_fused returns
 // cudaErrorNotSupported, before launching, when the page layout does not fit
 // its shared-memory plan.
 bool fused_supported(const spg_params& p, int append);
+// The whole step as one persistent launch with task queues (see
+// spg_sched.cu); launch_sched returns cudaErrorNotSupported, before
+// launching, when the parameters do not fit its plan.
+bool sched_supported(const spg_params& p, int append);
+cudaError_t launch_sched(const spg_params& p, const void* q, const void* k_pool,
+                         const void* v_pool, const void* k_scale, const void* v_scale,
+                         const int32_t* page_table, const int32_t* seq_lens, void* minmax,
+                         const uint8_t* sketch, const float* sketch_scale, const float* proj,
+                         int32_t* sel, int32_t* sel_cnt, float* out, float* lse, int append,
+                         const Workspace& ws, cudaStream_t stream);
 cudaError_t launch_fused(const spg_params& p, const void* q, const void* k_pool,
                          const void* v_pool, const void* k_scale, const void* v_scale,
                          const int32_t* page_table, const int32_t* seq_lens, void* minmax,

@@ -223,6 +223,53 @@ __global__ void __launch_bounds__(1024) k_topk(const SelectArgs a) {
               a.sel + static_cast<size_t>(unit) * a.n_sel, a.sel_cnt + unit, s_keys, s_t);
 }
 
+// The sketch selector's integer arithmetic laid bare (QSI steps 1-2): per
+// unit, the int8 index query (the same warp routine every scan uses) and the
+// exact int32 dot of the query codes with every token of every candidate
+// block (the same token routine as the block scores).  Grid: one CTA of 256
+// threads per (batch, kv-head).
+template <typename TQ>
+__global__ void __launch_bounds__(256) k_sketch_dots(const SelectArgs a, int32_t* qc_out,
+                                                      float* sq_out, int32_t* dots) {
+  constexpr int DS = 16;
+  __shared__ float s_qbar[256];
+  __shared__ float s_P[256 * DS];
+  __shared__ int s_qc[4];
+  __shared__ int s_bias;
+  pdl_wait();
+  const int unit = blockIdx.x, Hkv = a.Hkv, G = a.G, d = a.d, S = a.S;
+  const int b = unit / Hkv, h = unit % Hkv;
+  int L;
+  const int P = seq_pages(a, b, &L);
+  const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo);
+  for (int i = threadIdx.x; i < d * DS; i += blockDim.x) s_P[i] = a.proj[i];
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int qc4[4], code;
+    float sq;
+    sketch_index_query_warp<TQ>(static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hkv * G + h * G) * d,
+                                G, d, s_P, s_qbar, threadIdx.x, qc4, sq, &code);
+    if (threadIdx.x < DS) qc_out[static_cast<size_t>(unit) * DS + threadIdx.x] = code;
+    if (threadIdx.x == 0) {
+      sq_out[unit] = sq;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) s_qc[k] = qc4[k];
+      s_bias = sketch_query_bias(qc4);
+    }
+  }
+  __syncthreads();
+  const int qc[4] = {s_qc[0], s_qc[1], s_qc[2], s_qc[3]};
+  const int bias = s_bias;
+  const size_t base = static_cast<size_t>(unit) * a.MP * S;
+  for (size_t i = threadIdx.x; i < static_cast<size_t>(a.MP) * S; i += blockDim.x) {
+    const int blk = static_cast<int>(i / S);
+    int v = 0;
+    if (blk >= lo && blk < hi)
+      v = sketch_token_dot(__ldg(reinterpret_cast<const uint2*>(a.sketch + (base + i) * (DS / 2))), qc, bias);
+    dots[base + i] = v;
+  }
+}
+
 template <typename T>
 cudaError_t quest_typed(const spg_params& p, const SelectArgs& a, int fused, size_t smem_keys,
                         cudaStream_t st) {
@@ -299,6 +346,32 @@ cudaError_t launch_select(const spg_params& p, const void* q, const int32_t* pag
   e = ensure_smem(k_topk, tsmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_topk, dim3(p.batch * p.num_kv_heads), dim3(1024), tsmem, stream, a);
+}
+
+}  // namespace spg
+
+namespace spg {
+
+cudaError_t launch_sketch_dots(const spg_params& p, const void* q, const int32_t* seq_lens,
+                               const uint8_t* sketch, const float* proj, int32_t* qc, float* sq,
+                               int32_t* dots, int32_t* err, cudaStream_t stream) {
+  SelectArgs a{};
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.sketch = sketch;
+  a.proj = proj;
+  a.err = err;
+  a.Hkv = p.num_kv_heads;
+  a.G = p.num_q_heads / p.num_kv_heads;
+  a.S = p.page_size;
+  a.d = p.head_dim;
+  a.MP = p.max_pages_per_seq;
+  a.n_sink = p.n_sink_pages;
+  a.n_recent = p.n_recent_pages;
+  const dim3 grid(p.batch * p.num_kv_heads);
+  if (p.q_dtype == SPG_F16)
+    return launch_pdl(k_sketch_dots<__half>, grid, dim3(256), 0, stream, a, qc, sq, dots);
+  return launch_pdl(k_sketch_dots<__nv_bfloat16>, grid, dim3(256), 0, stream, a, qc, sq, dots);
 }
 
 }  // namespace spg

@@ -600,41 +600,67 @@ __device__ __forceinline__ int pack_i8x4(int a, int b, int c, int d) {
 }
 
 
-// Index query of the sketch selector for one kv-head group: the group mean
-// of the G query rows, projected through P (d x 16) and quantised to int8,
-// all in fp32 with one rounded product and one rounded add per step, in
-// channel order (the same rule as the key side).  Called by a whole CTA;
-// s_qbar holds d floats, s_P d*16 floats.  Leaves the codes packed for dp4a
-// in s_qc[4] (even 0-6, odd 1-7, even 8-14, odd 9-15) and the scale in *s_sq.
+// Exact int32 dot of one token's 16 int4 key codes (8 bytes) with the int8
+// index query (packed for dp4a in qc[4]; bias = sketch_query_bias(qc)):
+// QSI step 1, the integer product before any dequantisation.
+__device__ __forceinline__ int sketch_token_dot(uint2 w, const int* qc, int bias) {
+  const int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
+  return dot_int4x8_biased(w.y, qc[2], qc[3], dot);
+}
+
+// Index query of the sketch selector for one kv-head group, by one warp:
+// the group mean of the G query rows (summed in head order, then divided by
+// G), projected through P (d x 16, staged in shared memory) with one rounded
+// product and one rounded add per step in channel order (the rule of the key
+// side), and quantised to int8 with scale max|q~| / 127 (1 when zero), round
+// half to even.  s_qbar: d floats of shared memory for this warp.  Every lane
+// returns the codes packed for dp4a (even 0-6, odd 1-7, even 8-14, odd
+// 9-15) and the scale; lanes j < 16 also return code j in *code_j.
 template <typename TQ>
-__device__ void sketch_index_query(const TQ* qb, int G, int d, const float* proj, float* s_qbar,
-                                   float* s_P, int* s_qc, float* s_sq) {
+__device__ void sketch_index_query_warp(const TQ* qb, int G, int d, const float* s_P, float* s_qbar,
+                                        int lane, int (&qc4)[4], float& sq, int* code_j = nullptr) {
   constexpr int DS = 16;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+  for (int i = lane; i < d; i += 32) {
     float s = to_f32(qb[i]);
     for (int g = 1; g < G; ++g) s = __fadd_rn(s, to_f32(qb[static_cast<size_t>(g) * d + i]));
     s_qbar[i] = __fdiv_rn(s, static_cast<float>(G));
   }
+  __syncwarp();
+  float qt = 0.f;
+  if (lane < DS)
+    for (int i = 0; i < d; ++i) qt = __fadd_rn(qt, __fmul_rn(s_qbar[i], s_P[i * DS + lane]));
+  float am = fabsf(qt);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  sq = am > 0.f ? __fdiv_rn(am, 127.0f) : 1.0f;
+  const int qc = max(-127, min(127, static_cast<int>(rintf(__fdiv_rn(qt, sq)))));
+  if (code_j) *code_j = qc;
+  int c[DS];
+#pragma unroll
+  for (int j = 0; j < DS; ++j) c[j] = __shfl_sync(0xffffffffu, qc, j);
+  qc4[0] = pack_i8x4(c[0], c[2], c[4], c[6]);
+  qc4[1] = pack_i8x4(c[1], c[3], c[5], c[7]);
+  qc4[2] = pack_i8x4(c[8], c[10], c[12], c[14]);
+  qc4[3] = pack_i8x4(c[9], c[11], c[13], c[15]);
+  __syncwarp();  // s_qbar may be reused
+}
+
+// The same for a whole CTA: P staged into s_P (d*16 floats) by every
+// thread, then warp 0 builds the query; leaves the packed codes in s_qc[4]
+// and the scale in *s_sq.
+template <typename TQ>
+__device__ void sketch_index_query(const TQ* qb, int G, int d, const float* proj, float* s_qbar,
+                                   float* s_P, int* s_qc, float* s_sq) {
+  constexpr int DS = 16;
   for (int i = threadIdx.x; i < d * DS; i += blockDim.x) s_P[i] = proj[i];
   __syncthreads();
-  if (warp == 0) {
-    float qt = 0.f;
-    if (lane < DS)
-      for (int i = 0; i < d; ++i) qt = __fadd_rn(qt, __fmul_rn(s_qbar[i], s_P[i * DS + lane]));
-    float am = fabsf(qt);
+  if (threadIdx.x < 32) {
+    int qc4[4];
+    float sq;
+    sketch_index_query_warp<TQ>(qb, G, d, s_P, s_qbar, threadIdx.x, qc4, sq);
+    if (threadIdx.x == 0) {
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    const float sq = am > 0.f ? __fdiv_rn(am, 127.0f) : 1.0f;
-    const int qc = max(-127, min(127, static_cast<int>(rintf(__fdiv_rn(qt, sq)))));
-    int c[DS];
-#pragma unroll
-    for (int j = 0; j < DS; ++j) c[j] = __shfl_sync(0xffffffffu, qc, j);
-    if (lane == 0) {
-      s_qc[0] = pack_i8x4(c[0], c[2], c[4], c[6]);
-      s_qc[1] = pack_i8x4(c[1], c[3], c[5], c[7]);
-      s_qc[2] = pack_i8x4(c[8], c[10], c[12], c[14]);
-      s_qc[3] = pack_i8x4(c[9], c[11], c[13], c[15]);
+      for (int k = 0; k < 4; ++k) s_qc[k] = qc4[k];
       *s_sq = sq;
     }
   }
@@ -653,9 +679,7 @@ __device__ __forceinline__ float sketch_block_score(const uint2 (&wk)[4], int S,
   for (int k = 0; k < 4; ++k) {
     z[k] = -INFINITY;
     if (lane + 32 * k < S) {
-      int dot = dot_int4x8_biased(wk[k].x, qc[0], qc[1], -bias);
-      dot = dot_int4x8_biased(wk[k].y, qc[2], qc[3], dot);
-      z[k] = static_cast<float>(dot) * cz;
+      z[k] = static_cast<float>(sketch_token_dot(wk[k], qc, bias)) * cz;
       zmax = fmaxf(zmax, z[k]);
     }
   }
@@ -687,9 +711,7 @@ __device__ __forceinline__ void sketch_block_scores4(const uint8_t* tile, int rb
       z[r][k] = -INFINITY;
       if (r < nb && lane + 32 * k < S) {
         const uint2 w = *reinterpret_cast<const uint2*>(tile + r * rb + (lane + 32 * k) * 8);
-        int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
-        dot = dot_int4x8_biased(w.y, qc[2], qc[3], dot);
-        z[r][k] = static_cast<float>(dot) * cz[r] * kL2e;  // log2 domain
+        z[r][k] = static_cast<float>(sketch_token_dot(w, qc, bias)) * cz[r] * kL2e;  // log2 domain
         zmax[r] = fmaxf(zmax[r], z[r][k]);
       }
     }
@@ -731,9 +753,7 @@ __device__ __forceinline__ float sketch_block_score_lane(const uint8_t* blk, int
     int tt = t + rot;
     if (tt >= S) tt -= S;
     const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
-    int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
-    dot = dot_int4x8_biased(w.y, qc[2], qc[3], dot);
-    dmax = max(dmax, dot);
+    dmax = max(dmax, sketch_token_dot(w, qc, bias));
   }
   const float zmax = static_cast<float>(dmax) * cz * kL2e;
   float sum = 0.f;
@@ -741,9 +761,7 @@ __device__ __forceinline__ float sketch_block_score_lane(const uint8_t* blk, int
     int tt = t + rot;
     if (tt >= S) tt -= S;
     const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
-    int dot = dot_int4x8_biased(w.x, qc[0], qc[1], -bias);
-    dot = dot_int4x8_biased(w.y, qc[2], qc[3], dot);
-    sum += exp2f(static_cast<float>(dot) * cz * kL2e - zmax);
+    sum += exp2f(static_cast<float>(sketch_token_dot(w, qc, bias)) * cz * kL2e - zmax);
   }
   return (zmax + log2f(sum)) * kLn2;
 }

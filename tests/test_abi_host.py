@@ -74,6 +74,11 @@ def test_every_workload_validates(spg):
     (dict(num_q_heads=6), 2),                 # group of 3
     (dict(page_size=12), 1),
     (dict(page_size=256), 1),
+    (dict(page_size=8), 2),                   # valid, not built: tensor-core tiles are 16 tokens
+    (dict(page_size=128, token_budget=512), 2),  # fp16 K + V of a 128-token d128 page: 64 KB
+    (dict(page_size=128, token_budget=512, head_dim=64), 0),
+    (dict(page_size=64, token_budget=256), 0),
+    (dict(page_size=128, token_budget=512, selector="sketch", kv_dtype="i8"), 0),
     (dict(token_budget=100), 1),              # not a multiple of the page size
     (dict(token_budget=16), 1),               # budget below the forced pages
     (dict(n_sink_pages=-1), 1),
@@ -124,3 +129,33 @@ def test_binding_refuses_host_tensors(spg):
     t = torch.zeros(16)
     with pytest.raises(ValueError):
         spg.sparse_page_score(p, t, t, t, t, scores=t, ws=torch.zeros(16, dtype=torch.uint8))
+
+
+def test_step_kernel_queries(spg):
+    """Host-only: which kernel the decode step launches, and how many times.
+    The cluster kernel takes every benchmark workload in one launch (the
+    scheduled kernel when it is preferred); a page table past 8192 pages
+    takes the separate kernels."""
+    from synth import WORKLOADS
+
+    for w in WORKLOADS.values():
+        p = spg.make_params(batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                            head_dim=w.head_dim, page_size=w.page_size, num_phys_pages=1 << 16,
+                            max_pages_per_seq=w.max_pages_per_seq, kv_dtype=w.kv_dtype,
+                            q_dtype=w.q_dtype, selector=w.selector, token_budget=w.token_budget,
+                            n_sink_pages=w.n_sink, n_recent_pages=w.n_recent)
+        assert spg.step_kernel_name(p) == "k_fused", w.name
+        assert spg.step_launch_count(p) == 1
+    try:
+        spg.spg_set_step_kernel(spg.STEP_KERNEL_SCHED)
+        assert spg.step_kernel_name(p) == "k_sched"
+        assert spg.step_launch_count(p) == 1
+    finally:
+        spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
+    with pytest.raises(spg.SpgError):
+        spg.spg_set_step_kernel(7)
+    long = _valid(spg, max_pages_per_seq=9000, num_phys_pages=20000)
+    assert spg.step_kernel_name(long) == "k_quest_select+k_attn"
+    assert spg.step_launch_count(long) == 4
+    assert spg.step_kernel_name(_valid(spg, head_dim=48)) is None
+    assert spg.step_launch_count(_valid(spg, head_dim=48)) == 0

@@ -22,11 +22,32 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 
+# The single-launch step has two kernels: the persistent scheduled one (the
+# default where it applies) and the cluster-per-unit one.  Tests marked with
+# this parameter run through each.
+KERNELS = ["sched", "cluster"]
+
 
 def _spg():
     import query_aware_sparse_page_gb300 as spg
 
     return spg
+
+
+@pytest.fixture
+def step_kernel(request):
+    """Selects the single-launch step kernel for one test, then restores the default."""
+    spg = _spg()
+    name = getattr(request, "param", "sched")
+    spg.spg_set_step_kernel(spg.STEP_KERNEL_SCHED if name == "sched" else spg.STEP_KERNEL_CLUSTER)
+    yield name
+    spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
+
+
+def _expect_kernel(p, name):
+    spg = _spg()
+    k = spg.step_kernel_name(p)
+    assert k == ("k_sched" if name == "sched" else "k_fused"), k
 
 
 SMALL = {
@@ -44,14 +65,35 @@ SMALL = {
                           head_dim=64, seq_len=16 * 700 + 3, needles_per_head=8, n_sel_pages=40),
     "gqa2-f16": scaled(get_workload("tiny-quest-gqa4-1k"), num_q_heads=4, num_kv_heads=2, head_dim=128,
                        seq_len=2000, n_sel_pages=20, n_sink=2, n_recent=3),
+    # every other shape spg_validate accepts: int8 pools with a bf16 query or
+    # d = 64 (the CUDA-core int8 consumer), the sketch selector over 16-bit
+    # pools and at 128-token blocks, Quest at 32-, 64- and 128-token pages
+    "sals-bf16q": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                         seq_len=64 * 18 + 5, n_sel_pages=6, q_dtype="bf16"),
+    "sals-d64": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                       head_dim=64, seq_len=64 * 18 + 33, n_sel_pages=6),
+    "sals-s128-f16": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=4, num_kv_heads=2,
+                            head_dim=64, page_size=128, seq_len=128 * 12 + 100, n_sel_pages=5,
+                            kv_dtype="f16", q_dtype="f16"),
+    "sals-s128-i8": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                           page_size=128, seq_len=128 * 10 + 128, n_sel_pages=4),
+    "quest-s32": scaled(get_workload("llama2-7b-mha-32k"), num_q_heads=4, num_kv_heads=2,
+                        page_size=32, seq_len=32 * 150 + 7, n_sel_pages=20, needles_per_head=4),
+    "quest-s64-bf16": scaled(get_workload("gqa-serving-b8-4k-64k"), batch=3, num_q_heads=8, num_kv_heads=2,
+                             page_size=64, seq_range=(300, 5000), n_sel_pages=12),
+    "quest-s128-d64": scaled(get_workload("long-scan-b4-128k"), batch=2, num_q_heads=8, num_kv_heads=2,
+                             head_dim=64, page_size=128, seq_len=128 * 40 + 77, n_sel_pages=8,
+                             needles_per_head=4),
 }
 
 
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_small_workload_every_unit(name):
+def test_small_workload_every_unit(name, step_kernel):
     w = SMALL[name]
     inp = make_inputs(w, device=DEV)
     p, bufs, err = run_step(inp)
+    _expect_kernel(p, step_kernel)
     assert err == 0
     prm = oracle_params(w)
     for b in range(w.batch):
@@ -72,8 +114,9 @@ def test_separate_calls_equal_fused(name):
     assert_paths_agree(b1.out, b2.out, b1.lse, b2.lse, w.kv_dtype, inp.v_pool.float().abs().max())
 
 
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("name", ["tiny-ragged", "gqa-ragged", "sals-4x", "sals-6x-full-tail"])
-def test_decode_step_appends_then_attends(name):
+def test_decode_step_appends_then_attends(name, step_kernel):
     """sparse_decode_step = append the new token's metadata, select, attend."""
     spg = _spg()
     w = SMALL[name]
@@ -239,7 +282,8 @@ def test_sketch_append_equals_rebuild():
     assert torch.equal(a.sketch, r.sketch) and torch.equal(a.sketch_scale, r.sketch_scale)
 
 
-def test_edge_sequences():
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
+def test_edge_sequences(step_kernel):
     """Empty, one-token, page-aligned, and shorter-than-budget sequences."""
     w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=6, num_q_heads=8, num_kv_heads=2,
                seq_range=(1, 2), n_sel_pages=6)
@@ -254,7 +298,8 @@ def test_edge_sequences():
     assert (bufs.out[0] == 0).all() and torch.isneginf(bufs.lse[0]).all()
 
 
-def test_all_equal_scores_take_lowest_pages():
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
+def test_all_equal_scores_take_lowest_pages(step_kernel):
     """Identical pages tie everywhere: the lowest candidate pages win."""
     spg = _spg()
     w = scaled(get_workload("tiny-quest-gqa4-1k"), seq_len=16 * 40, n_sel_pages=7, needles_per_head=0)
@@ -296,8 +341,9 @@ def _integer_score_inputs(kind, n_pages=1200, n_sel=100):
     return w, inp
 
 
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("kind", ["three-values", "planted-ties", "wide-integers"])
-def test_exact_ties_across_the_cluster(kind):
+def test_exact_ties_across_the_cluster(kind, step_kernel):
     """Exact ties between pages scored in different CTAs: lower page index wins."""
     w, inp = _integer_score_inputs(kind)
     p, bufs, err = run_step(inp)
@@ -312,7 +358,8 @@ def test_exact_ties_across_the_cluster(kind):
         check_unit(inp, prm, bufs, 0, h, TOL_OUT[w.kv_dtype])
 
 
-def test_budget_of_only_forced_pages():
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
+def test_budget_of_only_forced_pages(step_kernel):
     """A budget equal to the forced pages selects no candidate."""
     w = scaled(SMALL["mha"], n_sel_pages=2)
     inp = make_inputs(w, device=DEV)
@@ -325,8 +372,9 @@ def test_budget_of_only_forced_pages():
         check_unit(inp, prm, bufs, 0, h, TOL_OUT[w.kv_dtype])
 
 
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("name", ["tiny", "long-d64-g8"])
-def test_needle_pages_selected(name):
+def test_needle_pages_selected(name, step_kernel):
     w = SMALL[name]
     inp = make_inputs(w, device=DEV)
     _, bufs, _ = run_step(inp)
@@ -335,7 +383,8 @@ def test_needle_pages_selected(name):
         assert pages <= set(gpu_selection(bufs, b, h))
 
 
-def test_bad_page_id_is_reported_not_read():
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
+def test_bad_page_id_is_reported_not_read(step_kernel):
     spg = _spg()
     w = SMALL["tiny"]
     inp = make_inputs(w, device=DEV)
@@ -367,11 +416,13 @@ FULL = ["llama2-7b-mha-32k", "gqa-serving-b8-4k-64k", "sals-int8-b16-10k-4x",
         "sals-int8-b16-10k-6x", "long-scan-b4-128k"]
 
 
+@pytest.mark.parametrize("step_kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_units(name):
+def test_full_size_sampled_units(name, step_kernel):
     w = get_workload(name)
     inp = make_inputs(w, device=DEV)
     p, bufs, err = run_step(inp)
+    _expect_kernel(p, step_kernel)
     assert err == 0
     prm = oracle_params(w)
     rng = np.random.default_rng(7)
@@ -394,3 +445,54 @@ def test_full_size_sampled_units(name):
             assert np.all(np.diff(s) > 0) and s[0] >= 0 and s[-1] == P - 1
             if w.n_sink:
                 assert s[0] == 0
+
+
+@pytest.mark.parametrize("name", ["gqa-ragged", "sals-4x", "mha"])
+def test_repeated_steps_on_one_workspace(name):
+    """The scheduled kernel leaves its queue counters and per-unit flags at
+    zero: steps launched back to back on one workspace, alternating with the
+    cluster kernel and with the separate kernels, give identical results."""
+    spg = _spg()
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    ref = spg.alloc_buffers(p, DEV)
+    spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 1,
+                                ref.minmax, ref.sketch, ref.sketch_scale, inp.proj, ref.ws)
+    b = spg.alloc_buffers(p, DEV)
+    if ref.minmax is not None:
+        b.minmax.copy_(ref.minmax)
+    else:
+        b.sketch.copy_(ref.sketch)
+        b.sketch_scale.copy_(ref.sketch_scale)
+
+    def step(bufs):
+        spg.sparse_decode_select_attend(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                        inp.page_table, inp.seq_lens, bufs.minmax, bufs.sketch,
+                                        bufs.sketch_scale, inp.proj, bufs.sel, bufs.sel_cnt,
+                                        bufs.out, bufs.lse, bufs.ws)
+
+    try:
+        spg.spg_set_step_kernel(spg.STEP_KERNEL_SCHED)
+        step(ref)
+        torch.cuda.synchronize()
+        for kernel in [spg.STEP_KERNEL_SCHED] * 3 + [spg.STEP_KERNEL_CLUSTER, spg.STEP_KERNEL_SCHED]:
+            spg.spg_set_step_kernel(kernel)
+            step(b)
+            if kernel == spg.STEP_KERNEL_CLUSTER:
+                spg.sparse_page_select(p, inp.q, inp.page_table, inp.seq_lens, b.minmax, b.sketch,
+                                       b.sketch_scale, inp.proj, b.sel, b.sel_cnt, b.ws)
+                spg.sparse_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale,
+                                            inp.v_scale, inp.page_table, inp.seq_lens, b.sel,
+                                            b.sel_cnt, b.out, b.lse, b.ws)
+                continue
+            torch.cuda.synchronize()
+            assert torch.equal(b.sel, ref.sel) and torch.equal(b.sel_cnt, ref.sel_cnt)
+            assert torch.equal(b.out, ref.out) and torch.equal(b.lse, ref.lse)
+        assert spg.spg_read_device_error(b.ws) == 0
+        # the workspace's queue counters are back at zero
+        hdr = b.ws[64:96].view(torch.int32).cpu()
+        assert int(hdr.abs().sum()) == 0, hdr.tolist()
+    finally:
+        spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
+
