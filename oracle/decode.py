@@ -36,6 +36,15 @@ class StepParams:
     selector: str  # "quest" | "sketch" | "all"
     head_dim: int
     softmax_scale: float = 0.0  # 0 -> 1/sqrt(head_dim)
+    top_p: float = 0.0  # adaptive budget: 0 = off (the fixed budget)
+    min_pages: int = 0  # adaptive budget: fewest candidate pages kept
+
+    @property
+    def tau(self) -> float:
+        """Temperature of the page-score softmax of the adaptive budget: the
+        sketch block score is already a log attention mass (1); the Quest
+        bound is on the unscaled dot product, so it takes the softmax scale."""
+        return 1.0 if self.selector == "sketch" else self.scale
 
     @property
     def scale(self) -> float:
@@ -126,6 +135,9 @@ def unit_selection(inp: StepInputs, prm: StepParams, b: int, h: int, scores=None
         return list(range(P))
     if scores is None:
         scores = unit_scores(inp, prm, b, h)
+    if prm.top_p > 0.0:
+        return select.select_pages_top_p(scores, P, prm.n_sel, prm.n_sink, prm.n_recent, prm.top_p,
+                                         prm.min_pages, prm.tau)
     return select.select_pages(scores, P, prm.n_sel, prm.n_sink, prm.n_recent)
 
 

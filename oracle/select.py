@@ -20,6 +20,8 @@ ascending page order.
 
 from __future__ import annotations
 
+import math
+
 
 def forced_pages(P: int, n_sink: int, n_recent: int) -> list[int]:
     f = set(range(min(n_sink, P))) | set(range(max(P - n_recent, 0), P))
@@ -36,4 +38,53 @@ def select_pages(scores, P: int, n_sel: int, n_sink: int, n_recent: int) -> list
     cand = [p for p in range(P) if p not in fset]
     k_top = max(n_sel - len(forced), 0)
     ranked = sorted(cand, key=lambda p: (-float(scores[p]), p))
+    return sorted(fset | set(ranked[:k_top]))
+
+
+def top_p_count(cand_scores, top_p: float, tau: float) -> int:
+    """Smallest k such that the k best candidates hold at least top_p of the
+    softmax mass of all candidates.
+
+    Source: "SequenceO1" close reading, §3.2 (STCA's relative threshold:
+    keep the leading items whose cumulative importance reaches the fraction
+    p of the total, p typically 0.8 to 0.95) and §4.2 (softmax of the sketch
+    scores, sorted descending, cumulative sum, at least one item kept).
+    cand_scores must already be in selection order (score descending, index
+    ascending); the weights are exp(tau * (s - max s)) in fp64.  Returns
+    len(cand_scores) when the running sum never reaches top_p * total (fp64
+    rounding at p = 1).
+    """
+    s = [float(x) for x in cand_scores]
+    if not s:
+        return 0
+    mx = max(s)
+    w = [math.exp(tau * (x - mx)) for x in s]
+    total = math.fsum(w)
+    acc = 0.0
+    for j, x in enumerate(w):
+        acc += x
+        if acc >= top_p * total:
+            return j + 1
+    return len(s)
+
+
+def select_pages_top_p(scores, P: int, n_sel: int, n_sink: int, n_recent: int, top_p: float,
+                       min_pages: int, tau: float) -> list[int]:
+    """Selected logical pages with the adaptive (top-p) budget, ascending.
+
+    The candidates are ranked as in select_pages; the fixed budget's k_top =
+    n_sel - |forced| (at most the candidates) caps the count; within it the
+    count is the top-p count of top_p_count, but at least min_pages
+    candidates (SequenceO1 §4.2 keeps at least one).  top_p <= 0 turns the
+    adaptive budget off (the fixed budget, as select_pages).
+    """
+    if top_p <= 0.0:
+        return select_pages(scores, P, n_sel, n_sink, n_recent)
+    forced = forced_pages(P, n_sink, n_recent)
+    fset = set(forced)
+    cand = [p for p in range(P) if p not in fset]
+    k_budget = min(max(n_sel - len(forced), 0), len(cand))
+    ranked = sorted(cand, key=lambda p: (-float(scores[p]), p))
+    k_p = top_p_count([scores[p] for p in ranked], top_p, tau)
+    k_top = min(k_budget, max(k_p, min(min_pages, k_budget)))
     return sorted(fset | set(ranked[:k_top]))

@@ -92,3 +92,68 @@ def test_planted_mistake_is_caught(rng, monkeypatch):
     monkeypatch.setattr(select, "select_pages", upper_wins)
     with pytest.raises(AssertionError):
         test_ties_go_to_lower_index(rng)
+
+
+# ---- adaptive (top-p) budget: SequenceO1 close reading §3.2 / §4.2 -----------
+
+def _mass(scores, pages, tau):
+    mx = max(scores)
+    w = {p: np.exp(tau * (scores[p] - mx)) for p in range(len(scores))}
+    return sum(w[p] for p in pages) / sum(w.values())
+
+
+def test_top_p_count_is_the_smallest_subset_reaching_p(rng):
+    """Brute force over every subset of a few candidates: the top-p count is
+    the fewest pages whose softmax mass reaches p, and the chosen pages carry
+    the largest mass among subsets of that size."""
+    for trial in range(150):
+        n = int(rng.integers(1, 9))
+        scores = rng.standard_normal(n) * float(rng.choice([0.3, 1.0, 4.0]))
+        tau = float(rng.choice([1.0, 0.5, 2.0]))
+        p = float(rng.uniform(0.05, 0.99))
+        sel = select.select_pages_top_p(scores, n, n, 0, 0, p, 0, tau)
+        m_star = min(len(c) for r in range(1, n + 1) for c in itertools.combinations(range(n), r)
+                     if _mass(scores, c, tau) >= p)
+        assert len(sel) == m_star
+        best = max(_mass(scores, c, tau) for c in itertools.combinations(range(n), m_star))
+        assert _mass(scores, sel, tau) == pytest.approx(best, rel=1e-12)
+
+
+def test_top_p_uniform_scores_closed_form():
+    # equal weights: the count is ceil(p * n); ties keep the lowest indices
+    for n, p, k in [(10, 0.45, 5), (10, 0.91, 10), (7, 0.2, 2), (100, 0.805, 81)]:
+        sel = select.select_pages_top_p(np.zeros(n), n, n, 0, 0, p, 0, 1.0)
+        assert sel == list(range(k))
+
+
+def test_top_p_one_dominant_page_floor_and_cap():
+    scores = np.array([0.0] * 30)
+    scores[17] = 12.0  # e^12 against 29: above 99.9 % of the mass
+    assert select.select_pages_top_p(scores, 30, 30, 0, 0, 0.99, 0, 1.0) == [17]
+    # the floor keeps at least min_pages candidates (the §4.2 listing keeps one)
+    assert select.select_pages_top_p(scores, 30, 30, 0, 0, 0.99, 3, 1.0) == [0, 1, 17]
+    # p = 1 takes every candidate within the budget; the budget caps the count
+    assert len(select.select_pages_top_p(scores, 30, 30, 0, 0, 1.0, 0, 1.0)) == 30
+    assert len(select.select_pages_top_p(np.zeros(30), 30, 6, 1, 2, 0.9, 0, 1.0)) == 6
+
+
+def test_top_p_forced_pages_and_off_switch(rng):
+    for trial in range(50):
+        P = int(rng.integers(1, 60))
+        n_sink, n_recent = int(rng.integers(0, 3)), int(rng.integers(0, 3))
+        n_sel = n_sink + n_recent + int(rng.integers(0, 20))
+        scores = rng.standard_normal(P) * 3
+        fixed = select.select_pages(scores, P, n_sel, n_sink, n_recent)
+        assert select.select_pages_top_p(scores, P, n_sel, n_sink, n_recent, 0.0, 0, 1.0) == fixed
+        adapt = select.select_pages_top_p(scores, P, n_sel, n_sink, n_recent, 0.8, 1, 1.0)
+        forced = set(select.forced_pages(P, n_sink, n_recent))
+        assert forced <= set(adapt) and set(adapt) <= set(fixed) and adapt == sorted(adapt)
+
+
+def test_top_p_temperature_is_a_score_scale(rng):
+    for trial in range(30):
+        P = int(rng.integers(2, 40))
+        s = rng.standard_normal(P)
+        a = select.select_pages_top_p(s, P, P, 0, 0, 0.7, 0, 0.5)
+        b = select.select_pages_top_p(s * 0.5, P, P, 0, 0, 0.7, 0, 1.0)
+        assert a == b
