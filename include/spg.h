@@ -85,7 +85,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st* spg_stream_t; /* a cudaStream_t */
 
-#define SPG_ABI_VERSION 1
+#define SPG_ABI_VERSION 2
 
 typedef enum {
   SPG_OK = 0,
@@ -130,6 +130,17 @@ typedef struct spg_params {
                                 selector needs >= 1 (the open tail block) */
   int32_t sketch_dim;        /* ds = 16 for SPG_SEL_SKETCH_INT4, else ignored */
   float softmax_scale;       /* 0 => 1/sqrt(head_dim) */
+  /* Adaptive budget (SequenceO1 close reading §3.2 / §4.2: keep the leading
+   * pages whose cumulative softmax mass of page scores reaches top_p).  0 =
+   * off: the token budget fixes the count.  In (0, 1]: of the candidates,
+   * in (score desc, page asc) order, keep the smallest prefix whose share
+   * of exp(tau * (s - max s)) over all candidates reaches top_p (tau = 1
+   * for the sketch selector, whose score is a log block mass; the softmax
+   * scale for Quest), at least min(min_pages, cap) and at most the cap
+   * n_sel - forced pages.  Weights and sums in fp32, in a fixed order.
+   * Needs n_sel <= 1024 (SPG_EUNSUPPORTED beyond); ignored by SPG_SEL_ALL. */
+  float top_p;
+  int32_t min_pages;         /* adaptive budget: fewest candidate pages kept (>= 0) */
 } spg_params;
 
 /* Library ABI version (SPG_ABI_VERSION of the build). */

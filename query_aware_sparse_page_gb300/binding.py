@@ -48,6 +48,8 @@ class spg_params(ctypes.Structure):
         ("n_recent_pages", c_int32),
         ("sketch_dim", c_int32),
         ("softmax_scale", c_float),
+        ("top_p", c_float),
+        ("min_pages", c_int32),
     ]
 
     def __repr__(self):
@@ -57,7 +59,7 @@ class spg_params(ctypes.Structure):
 def make_params(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_phys_pages,
                 max_pages_per_seq, kv_dtype="f16", q_dtype=None, selector="quest",
                 token_budget=0, n_sink_pages=0, n_recent_pages=0, sketch_dim=16,
-                softmax_scale=0.0) -> spg_params:
+                softmax_scale=0.0, top_p=0.0, min_pages=0) -> spg_params:
     kv = _DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
     if q_dtype is None:
         q_dtype = kv if kv != I8 else F16
@@ -65,7 +67,7 @@ def make_params(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_phys_
     sel = _SELECTORS[selector] if isinstance(selector, str) else int(selector)
     return spg_params(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_phys_pages,
                       max_pages_per_seq, kv, qd, sel, token_budget, n_sink_pages, n_recent_pages,
-                      sketch_dim, softmax_scale)
+                      sketch_dim, softmax_scale, top_p, min_pages)
 
 
 def _load():

@@ -198,6 +198,7 @@ spg_status spg_validate(const spg_params* p) {
   if (p->kv_dtype != SPG_I8 && p->q_dtype != p->kv_dtype) return SPG_EINVAL;
   if (p->selector < SPG_SEL_QUEST || p->selector > SPG_SEL_ALL) return SPG_EINVAL;
   if (!(p->softmax_scale >= 0.f) || std::isinf(p->softmax_scale)) return SPG_EINVAL;
+  if (!(p->top_p >= 0.f && p->top_p <= 1.f) || p->min_pages < 0) return SPG_EINVAL;
   if (p->selector != SPG_SEL_ALL) {
     if (p->n_sink_pages < 0 || p->n_recent_pages < 0) return SPG_EINVAL;
     if (p->token_budget < p->page_size || p->token_budget % p->page_size) return SPG_EINVAL;
@@ -224,6 +225,10 @@ spg_status spg_validate(const spg_params* p) {
   if (p->selector != SPG_SEL_ALL && p->max_pages_per_seq > spg::kMaxTopkPages)
     return SPG_EUNSUPPORTED;
   if (p->max_pages_per_seq > spg::kMaxSplits * 1024) return SPG_EUNSUPPORTED;
+  // the adaptive budget runs where the selection's keys sit in shared memory
+  if (p->selector != SPG_SEL_ALL && p->top_p > 0.f &&
+      (spg::n_sel_pages(*p) > spg::kMaxTopPPages || p->max_pages_per_seq > 8192))
+    return SPG_EUNSUPPORTED;
   return SPG_OK;
 }
 

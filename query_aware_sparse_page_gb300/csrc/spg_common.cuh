@@ -19,6 +19,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 128;  // split-K partials per (batch, q-head) held in the workspace
 constexpr int kMaxTopkPages = 49152;  // candidate keys of one (batch, kv-head) kept in shared memory
+constexpr int kMaxTopPPages = 1024;   // largest page budget of the adaptive (top-p) selection
 
 // ---- element conversions -------------------------------------------------
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
@@ -384,6 +385,11 @@ template <typename T>
 __host__ __device__ __forceinline__ int meta_swz(int e, int p) {
   constexpr int EPC = 16 / static_cast<int>(sizeof(T));
   return ((e / EPC) ^ (p & 7)) * EPC + (e % EPC);
+}
+
+// the score of a key (inverse of score_key)
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // order-preserving map of an fp32 score to uint32 (larger float -> larger key);

@@ -84,6 +84,8 @@ struct FusedArgs {
   float* lse;
   int32_t* err;
   int Hkv, S, MP, n_phys, n_sink, n_recent, n_sel, stages, rows_per_stage, append;
+  float top_p, tau;  // adaptive budget (top_p 0: off)
+  int min_pages;
   int cluster, pages_per_stage;
   uint32_t stage_bytes, row_bytes, page_bytes, ring_bytes, keys_off, sel_off, att_off;
   uint32_t pt_off;  // leader: the unit's page-table row, when it fits (0: not cached)
@@ -421,10 +423,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   if (rank == 0) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int nf = P - nc;
-    const int k_top = min(max(a.n_sel - nf, 0), nc);
+    int k_top = min(max(a.n_sel - nf, 0), nc);
     for (int i = tid; i < lo; i += nt) s_sel[i] = i;
-    for (int j = tid; j < P - hi; j += nt) s_sel[lo + k_top + j] = hi + j;
-    const int count = lo + k_top + (P - hi);
     if (k_top == nc) {
       for (int i = tid; i < nc; i += nt) s_sel[lo + i] = lo + i;
     } else if (k_top > 0) {
@@ -442,6 +442,18 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       __syncthreads();
       block_topk(s_keys, nc, k_top, lo, s_sel + lo, tk, true, true);
     }
+    if (a.top_p > 0.f && k_top > 0) {
+      // the adaptive budget trims the chosen candidates (the ring is idle:
+      // its scratch follows the top-k state)
+      __syncthreads();
+      uint32_t* tps = reinterpret_cast<uint32_t*>(ring + ((sizeof(TopkShared) + 127) & ~size_t(127)));
+      k_top = topp_trim(s_keys, nc, s_sel + lo, k_top, lo, a.tau, a.top_p, a.min_pages, tps,
+                        reinterpret_cast<int*>(tps + kTopPScratchWords),
+                        reinterpret_cast<float*>(tps + kTopPScratchWords + 40));
+    }
+    __syncthreads();
+    for (int j = tid; j < P - hi; j += nt) s_sel[lo + k_top + j] = hi + j;
+    const int count = lo + k_top + (P - hi);
     __syncthreads();
     if (a.pt_off != 0 && !mbar_wait_bounded(&s_ptbar, 0) && tid == 0)
       record_error(a.err, SPG_DEVERR_TIMEOUT);
@@ -630,6 +642,8 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   if (stages > kMaxStages) return cudaErrorNotSupported;
   size_t ring = static_cast<size_t>(stages) * sb;
   ring = max(ring, sizeof(TopkShared));
+  if (p.top_p > 0.f)  // the adaptive budget's scratch after the top-k state
+    ring = max(ring, ((sizeof(TopkShared) + 127) & ~size_t(127)) + sizeof(uint32_t) * (kTopPScratchWords + 80));
   ring = max(ring, sizeof(float) * kConsumerWarps * G * (D + 2));
   ring = (ring + 127) & ~static_cast<size_t>(127);
   const size_t meta = sizeof(uint64_t) * 2 * kMaxStages +
@@ -786,6 +800,9 @@ cudaError_t launch_fused(const spg_params& p, const void* q, const void* k_pool,
                                             : 1.0f / sqrtf(static_cast<float>(p.head_dim));
   a.scale_log2 = scale * kLog2e;
   a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(p.head_dim));
+  a.top_p = p.top_p;
+  a.min_pages = p.min_pages;
+  a.tau = p.selector == SPG_SEL_SKETCH_INT4 ? 1.0f : scale;
   switch (p.kv_dtype) {
     case SPG_F16:
       return fused_dispatch<__half, __half>(p, a, stream);

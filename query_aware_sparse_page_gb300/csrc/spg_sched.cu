@@ -113,10 +113,12 @@ struct SchedArgs {
   int units, R, PPS, SPW, stages, n_selectors;
   uint32_t stage_bytes, row_bytes, page_bytes, qbytes;
   uint32_t off_qbuf, off_merge;                            // worker layout
-  uint32_t off_spt, off_ssel, off_topk, off_sqbar, off_sP;  // selector layout
+  uint32_t off_spt, off_ssel, off_topk, off_sqbar, off_sP, off_tps;  // selector layout
   uint32_t off_fixed;                                       // both roles
   int pt_cached;
   float scale_log2, inv_sqrt_d;
+  float top_p, tau;  // adaptive budget (top_p 0: off)
+  int min_pages;
 };
 
 // fixed region (after the role-specific union)
@@ -150,7 +152,10 @@ __device__ __forceinline__ BInfo binfo(int L, int S, int n_sink, int n_recent, i
   r.cnt = r.lo + r.k_top + (r.P - r.hi);
   return r;
 }
-__device__ __forceinline__ bool needs_scan(const BInfo& i) { return i.k_top > 0 && i.k_top < i.nc; }
+// a unit's candidates are scored when the top-k or the adaptive budget needs them
+__device__ __forceinline__ bool needs_scan(const BInfo& i, bool adapt) {
+  return i.k_top > 0 && (i.k_top < i.nc || adapt);
+}
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
         }
         f.L[b] = L;
         const BInfo bi = binfo(L, S, a.n_sink, a.n_recent, a.n_sel);
-        ns = needs_scan(bi) ? (bi.nc + kScanGroup * R - 1) / (kScanGroup * R) * Hkv : 0;
+        ns = needs_scan(bi, a.top_p > 0.f) ? (bi.nc + kScanGroup * R - 1) / (kScanGroup * R) * Hkv : 0;
         na = (bi.cnt + PPT - 1) / PPT * Hkv;
       }
       int is = ns, ia = na;
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
         u = __shfl_sync(0xffffffffu, u, 0);
         if (u >= a.units) break;
         const int b = u / Hkv, h = u % Hkv;
-        if (!needs_scan(binfo(f.L[b], S, a.n_sink, a.n_recent, a.n_sel))) continue;
+        if (!needs_scan(binfo(f.L[b], S, a.n_sink, a.n_recent, a.n_sel), a.top_p > 0.f)) continue;
         const TQ* qb = static_cast<const TQ*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D;
         int c[4];
         float sq;
@@ -347,8 +352,9 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
       if (u >= a.units) break;
       const int b = u / Hkv, h = u % Hkv;
       const BInfo bi = binfo(f.L[b], S, a.n_sink, a.n_recent, a.n_sel);
-      const int lo = bi.lo, hi = bi.hi, nc = bi.nc, k_top = bi.k_top, count = bi.cnt, P = bi.P;
-      const bool scan = needs_scan(bi);
+      const int lo = bi.lo, hi = bi.hi, nc = bi.nc, P = bi.P;
+      int k_top = bi.k_top;
+      const bool scan = needs_scan(bi, a.top_p > 0.f);
       const bool pt_smem = a.pt_cached && P > 0;
       if (pt_smem && tid == 0) {
         // the unit's page-table row, while the scan runs
@@ -400,12 +406,22 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
           tk.kmax = mx;
         }
         __syncthreads();
-        block_topk(s_keys, nc, k_top, lo, s_sel + lo, tk, true, true);
+        if (k_top < nc)
+          block_topk(s_keys, nc, k_top, lo, s_sel + lo, tk, true, true);
       }
       for (int i = tid; i < lo; i += nt) s_sel[i] = i;
-      for (int j = tid; j < P - hi; j += nt) s_sel[lo + k_top + j] = hi + j;
       if (k_top == nc)
         for (int i = tid; i < nc; i += nt) s_sel[lo + i] = lo + i;
+      if (scan && a.top_p > 0.f) {  // the adaptive budget trims the chosen candidates
+        __syncthreads();
+        uint32_t* tps = reinterpret_cast<uint32_t*>(smem + a.off_tps);
+        k_top = topp_trim(s_keys, nc, s_sel + lo, k_top, lo, a.tau, a.top_p, a.min_pages, tps,
+                          reinterpret_cast<int*>(tps + kTopPScratchWords),
+                          reinterpret_cast<float*>(tps + kTopPScratchWords + 40));
+      }
+      __syncthreads();
+      for (int j = tid; j < P - hi; j += nt) s_sel[lo + k_top + j] = hi + j;
+      const int count = lo + k_top + (P - hi);
       __syncthreads();
       if (pt_smem) {
         if (!mbar_wait_bounded(&f.ptbar, ptphase) && tid == 0) set_abort(a);
@@ -575,11 +591,16 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
         const int per_head = (bi.cnt + PPT - 1) / PPT;
         const int loc = t - f.apref[b], h = loc / per_head, split = loc % per_head;
         const int u = b * Hkv + h;
-        const int p0 = split * PPT, p1 = min(p0 + PPT, bi.cnt);
+        const int p0 = split * PPT;
+        int p1 = min(p0 + PPT, bi.cnt);
         bool rdy = true;
         if (lane == 0) rdy = spin_geq(a, ready + u, 1);
         rdy = __shfl_sync(0xffffffffu, rdy ? 1 : 0, 0) != 0;
-        if (rdy) (void)ld_acquire(ready + u);
+        if (rdy) {
+          (void)ld_acquire(ready + u);
+          // the adaptive budget may have kept fewer pages than the fixed one
+          if (a.top_p > 0.f) p1 = min(p1, __ldcg(a.sel_cnt + u));
+        }
         const int2* sl = a.slices + static_cast<size_t>(u) * a.n_sel;
         for (int j = 0; j < CW * SPW; ++j) {
           const int slot = k % STAGES;
@@ -841,7 +862,9 @@ cudaError_t sched_typed(const spg_params& p, SchedArgs a, cudaStream_t st) {
   const size_t off_topk = (off_ssel + sizeof(int) * n_sel + 127) & ~size_t(127);
   const size_t off_sP = 0;  // index-query phase, before the keys are loaded
   const size_t off_sqbar = (sizeof(float) * D * 16 + 127) & ~size_t(127);
-  const size_t sel_end = std::max(off_topk + sizeof(TopkShared), off_sqbar + sizeof(float) * D * (kThreads / 32));
+  const size_t off_tps = (off_topk + sizeof(TopkShared) + 127) & ~size_t(127);
+  const size_t sel_end = std::max(off_tps + (p.top_p > 0.f ? sizeof(uint32_t) * (kTopPScratchWords + 80) : 0),
+                                  off_sqbar + sizeof(float) * D * (kThreads / 32));
   const size_t off_fixed = (std::max(worker_end, sel_end) + 127) & ~size_t(127);
   const size_t smem = 1024 + off_fixed + sizeof(FixedSmem);
   if (smem > 227u * 1024u) return cudaErrorNotSupported;
@@ -904,6 +927,7 @@ cudaError_t sched_typed(const spg_params& p, SchedArgs a, cudaStream_t st) {
   a.off_topk = static_cast<uint32_t>(off_topk);
   a.off_sP = static_cast<uint32_t>(off_sP);
   a.off_sqbar = static_cast<uint32_t>(off_sqbar);
+  a.off_tps = static_cast<uint32_t>(off_tps);
   a.off_fixed = static_cast<uint32_t>(off_fixed);
   a.pt_cached = p.max_pages_per_seq % 4 == 0 ? 1 : 0;
 
@@ -988,6 +1012,9 @@ cudaError_t launch_sched(const spg_params& p, const void* q, const void* k_pool,
                                             : 1.0f / sqrtf(static_cast<float>(p.head_dim));
   a.scale_log2 = scale * kLog2e;
   a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(p.head_dim));
+  a.top_p = p.top_p;
+  a.min_pages = p.min_pages;
+  a.tau = p.selector == SPG_SEL_SKETCH_INT4 ? 1.0f : scale;
   if (p.selector == SPG_SEL_QUEST) {
     switch (p.kv_dtype) {
       case SPG_F16:

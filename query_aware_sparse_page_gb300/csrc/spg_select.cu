@@ -50,36 +50,51 @@ struct SelectArgs {
   int32_t* err;
   int Hkv, G, S, d, MP, n_phys, n_sink, n_recent, n_sel;
   float inv_sqrt_d;
+  float top_p, tau;  // adaptive budget (top_p 0: off)
+  int min_pages;
 };
 
 // Selection of one unit from its scores row (global, written by this launch
-// or the previous one): forced sinks, the exact top-k candidates, forced
-// recent pages, then -1 padding; sel_cnt.
+// or the previous one): forced sinks, the exact top-k candidates (trimmed by
+// the adaptive budget when top_p > 0; tps: its shared-memory scratch),
+// forced recent pages, then -1 padding; sel_cnt.
 template <int MAXN>
 __device__ void select_unit(const float* srow, int P, int lo, int hi, int n_sel, int32_t* out,
-                            int32_t* cnt_out, uint32_t* s_keys, TopkSmem<MAXN>& t) {
+                            int32_t* cnt_out, uint32_t* s_keys, TopkSmem<MAXN>& t, float top_p,
+                            float tau, int min_pages, uint32_t* tps) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int nc = hi - lo, nf = P - nc;
-  const int k_top = min(max(n_sel - nf, 0), nc);
+  int k_top = min(max(n_sel - nf, 0), nc);
   for (int i = tid; i < lo; i += nt) out[i] = i;
+  if (k_top > 0) {
+    if (k_top == nc && top_p <= 0.f) {
+      for (int i = tid; i < nc; i += nt) out[lo + i] = lo + i;
+    } else {
+      for (int i = tid; i < nc; i += nt) s_keys[i] = score_key(__ldcg(srow + lo + i));
+      __syncthreads();
+      if (k_top == nc)
+        for (int i = tid; i < nc; i += nt) out[lo + i] = lo + i;
+      else
+        block_topk(s_keys, nc, k_top, lo, out + lo, t);
+      if (top_p > 0.f) {
+        __syncthreads();
+        k_top = topp_trim(s_keys, nc, out + lo, k_top, lo, tau, top_p, min_pages, tps,
+                          reinterpret_cast<int*>(tps + kTopPScratchWords),
+                          reinterpret_cast<float*>(tps + kTopPScratchWords + 40));
+      }
+    }
+  }
+  __syncthreads();
   for (int j = tid; j < P - hi; j += nt) out[lo + k_top + j] = hi + j;
   const int count = lo + k_top + (P - hi);
   for (int i = count + tid; i < n_sel; i += nt) out[i] = -1;
   if (tid == 0) *cnt_out = count;
-  if (k_top == 0) return;
-  if (k_top == nc) {
-    for (int i = tid; i < nc; i += nt) out[lo + i] = lo + i;
-    return;
-  }
-  for (int i = tid; i < nc; i += nt) s_keys[i] = score_key(__ldcg(srow + lo + i));
-  __syncthreads();
-  block_topk(s_keys, nc, k_top, lo, out + lo, t);
 }
 
 // Arrival of a scoring CTA; the last one of its unit selects the unit's pages.
 __device__ __forceinline__ void arrive_and_select(const SelectArgs& a, int unit, int P, int lo,
                                                   int hi, uint32_t* s_keys, TopkShared& t,
-                                                  int* s_last) {
+                                                  int* s_last, uint32_t* tps) {
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) *s_last = atomicAdd(&a.counters[unit], 1) == static_cast<int>(gridDim.x) - 1;
@@ -87,7 +102,8 @@ __device__ __forceinline__ void arrive_and_select(const SelectArgs& a, int unit,
   if (!*s_last) return;
   __threadfence();
   select_unit(a.scores + static_cast<size_t>(unit) * a.MP, P, lo, hi, a.n_sel,
-              a.sel + static_cast<size_t>(unit) * a.n_sel, a.sel_cnt + unit, s_keys, t);
+              a.sel + static_cast<size_t>(unit) * a.n_sel, a.sel_cnt + unit, s_keys, t, a.top_p,
+              a.tau, a.min_pages, tps);
   if (threadIdx.x == 0) a.counters[unit] = 0;  // ready for the next call
 }
 
@@ -155,7 +171,7 @@ __global__ void __launch_bounds__(128) k_quest_select(const SelectArgs a, int fu
     }
   }
   pdl_trigger();
-  if (fused) arrive_and_select(a, unit, P, lo, hi, s_keys, s_t, &s_last);
+  if (fused) arrive_and_select(a, unit, P, lo, hi, s_keys, s_t, &s_last, reinterpret_cast<uint32_t*>(rows));
 }
 
 // Sketch scores (+ fused selection): grid (ceil(MP/8), B*Hkv), 256 threads,
@@ -203,7 +219,7 @@ __global__ void __launch_bounds__(256) k_sketch_select(const SelectArgs a, int f
     if (lane == 0) a.scores[static_cast<size_t>(unit) * a.MP + blk] = score;
   }
   pdl_trigger();
-  if (fused) arrive_and_select(a, unit, P, lo, hi, s_keys, s_t, &s_last);
+  if (fused) arrive_and_select(a, unit, P, lo, hi, s_keys, s_t, &s_last, reinterpret_cast<uint32_t*>(s_P));
 }
 
 // Selection alone, for page tables too long to select inside the scoring
@@ -220,7 +236,8 @@ __global__ void __launch_bounds__(1024) k_topk(const SelectArgs a) {
   const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo);
   pdl_trigger();
   select_unit(a.scores + static_cast<size_t>(unit) * a.MP, P, lo, hi, a.n_sel,
-              a.sel + static_cast<size_t>(unit) * a.n_sel, a.sel_cnt + unit, s_keys, s_t);
+              a.sel + static_cast<size_t>(unit) * a.n_sel, a.sel_cnt + unit, s_keys, s_t, 0.f, 1.f,
+              0, nullptr);  // the adaptive budget is limited to tables of <= 8192 pages
 }
 
 // The sketch selector's integer arithmetic laid bare (QSI steps 1-2): per
@@ -320,6 +337,11 @@ cudaError_t launch_select(const spg_params& p, const void* q, const int32_t* pag
   a.n_recent = p.n_recent_pages;
   a.n_sel = n_sel_pages(p);
   a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(p.head_dim));
+  a.top_p = p.top_p;
+  a.min_pages = p.min_pages;
+  a.tau = p.selector == SPG_SEL_SKETCH_INT4
+              ? 1.0f
+              : (p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf(static_cast<float>(p.head_dim)));
   const int fused = (sel != nullptr && p.max_pages_per_seq <= kFusedTopkMaxPages) ? 1 : 0;
   const size_t smem = fused ? sizeof(uint32_t) * p.max_pages_per_seq : 0;
   cudaError_t e;

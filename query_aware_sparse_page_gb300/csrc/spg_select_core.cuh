@@ -453,6 +453,104 @@ __device__ __forceinline__ void block_topk(const uint32_t* __restrict__ keys, in
   __syncthreads();
 }
 
+// Adaptive budget (SequenceO1 close reading §3.2: keep the leading items
+// whose cumulative importance reaches the fraction p of the total; §4.2:
+// softmax of the scores, sorted, cumulative sum, at least one kept).  sel[0,
+// k_budget) holds the candidates the fixed budget chose (ascending page ids,
+// page p's key at keys[p - base]); keys[0, nc) are every candidate's keys.
+// Keeps the smallest prefix of the chosen, in (score desc, page asc) order,
+// whose weights exp(tau (s - max s)) add up to at least top_p of the weights
+// of all nc candidates, and at least min(k_min, k_budget) of them; rewrites
+// sel[0, k) ascending and returns k.  Weights and sums in fp32, each sum in a
+// fixed order (a thread's run, then a block scan), so the count does not
+// depend on timing.  k_budget <= kMaxTopPPages; scratch: kTopPScratchWords
+// words of shared memory; s_wi, s_wf: 36 words each; blockDim.x a multiple
+// of 32.  Every thread calls it.
+constexpr int kTopPScratchWords = 3 * kMaxTopPPages;
+
+template <typename SelT>
+__device__ int topp_trim(const uint32_t* keys, int nc, SelT* sel, int k_budget, int base, float tau,
+                         float top_p, int k_min, uint32_t* scratch, int* s_wi, float* s_wf) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  if (k_budget <= 0) return 0;
+  // p = 1: no proper prefix holds all the mass (every weight is positive),
+  // so the whole budget stays; fp32 sums in two orders cannot show that
+  // when a few pages dominate, so it is taken from the definition
+  if (top_p >= 1.f) return k_budget;
+  uint32_t* ck = scratch;                                        // [k_budget] chosen keys
+  float* w = reinterpret_cast<float*>(scratch + kMaxTopPPages);  // [k_budget] weights by rank
+  int* rk = reinterpret_cast<int*>(scratch + 2 * kMaxTopPPages); // [k_budget] rank of each
+  // the largest key (every chosen key set is a top set: it holds the max)
+  uint32_t kmx = 0u;
+  for (int i = tid; i < k_budget; i += nt) {
+    const uint32_t x = keys[static_cast<int>(sel[i]) - base];
+    ck[i] = x;
+    kmx = max(kmx, x);
+  }
+  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  if (lane == 0) s_wi[warp] = static_cast<int>(kmx);
+  __syncthreads();
+  uint32_t m = 0u;
+  for (int w2 = 0; w2 < nw; ++w2) m = max(m, static_cast<uint32_t>(s_wi[w2]));
+  const float smax = key_score(m);
+  // total weight of every candidate: a strided run per thread, then a fixed tree
+  float z = 0.f;
+  for (int i = tid; i < nc; i += nt) z += expf(tau * (key_score(keys[i]) - smax));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  __syncthreads();  // s_wi read above
+  if (lane == 0) s_wf[warp] = z;
+  // the rank of each chosen key among the chosen (key desc, page asc)
+  for (int i = tid; i < k_budget; i += nt) {
+    const uint32_t x = ck[i];
+    int r = 0;
+    for (int j = 0; j < k_budget; ++j) {
+      const uint32_t y = ck[j];
+      r += (y > x) || (y == x && j < i);
+    }
+    w[r] = expf(tau * (key_score(x) - smax));
+    rk[i] = r;
+  }
+  __syncthreads();
+  float Z = 0.f;
+  for (int w2 = 0; w2 < nw; ++w2) Z += s_wf[w2];
+  const float thr = top_p * Z;
+  __syncthreads();  // every thread has read the warp sums before the scan reuses them
+  // prefix sums of the weights in rank order: thread t owns ranks [r0, r1)
+  const int per = (k_budget + nt - 1) / nt;
+  const int r0 = min(k_budget, tid * per), r1 = min(k_budget, r0 + per);
+  float loc = 0.f;
+  for (int r = r0; r < r1; ++r) loc += w[r];
+  float pre = block_exclusive_scan_t<float>(loc, s_wf, s_wf + 32);
+  int below = 0;  // ranks whose running sum (through them) stays under top_p * Z
+  for (int r = r0; r < r1; ++r) {
+    pre += w[r];
+    below += pre < thr;
+  }
+  const int n_below = block_exclusive_scan(below, s_wi, s_wi + 32) + below;  // inclusive at the last thread
+  if (tid == nt - 1) s_wi[33] = n_below;
+  __syncthreads();
+  const int k_p = min(s_wi[33] + 1, k_budget);
+  const int k = min(k_budget, max(k_p, min(k_min, k_budget)));
+  // keep the chosen with rank < k, ascending (sel order): one block scan
+  SelT keep_id[1];
+  for (int i0 = 0; i0 < k_budget; i0 += nt) {  // block-uniform rounds
+    const int i = i0 + tid;
+    bool keep = false;
+    if (i < k_budget) {
+      keep = rk[i] < k;
+      keep_id[0] = sel[i];
+    }
+    __syncthreads();  // every entry of this round read before any is moved
+    const int before = i0 == 0 ? 0 : s_wi[34];
+    const int pos = block_exclusive_scan(keep ? 1 : 0, s_wi, s_wi + 32);
+    if (keep) sel[before + pos] = keep_id[0];
+    if (tid == nt - 1) s_wi[34] = before + pos + (keep ? 1 : 0);
+    __syncthreads();
+  }
+  return k;
+}
+
 using TopkShared = TopkSmem<8192>;
 static_assert(alignof(TopkShared) >= 16 && alignof(TopkSmem<kMaxTopkPages>) >= 16,
               "16-byte accesses to the histogram");

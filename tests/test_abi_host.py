@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(spg):
 
 
 def test_abi_version_and_status_strings(spg):
-    assert spg.spg_abi_version() == 1
+    assert spg.spg_abi_version() == 2
     assert spg.status_str(0) == "ok"
     assert spg.status_str(4) == "workspace too small"
     assert spg.status_str(99) == "unknown status"
@@ -89,6 +89,11 @@ def test_every_workload_validates(spg):
     (dict(softmax_scale=-1.0), 1),
     (dict(max_pages_per_seq=100000), 2),      # beyond the shared-memory top-k
     (dict(batch=0), 1),
+    (dict(top_p=1.5), 1),
+    (dict(top_p=-0.1), 1),
+    (dict(min_pages=-1), 1),
+    (dict(top_p=0.9, min_pages=2), 0),
+    (dict(top_p=0.9, token_budget=16 * 1025, max_pages_per_seq=2048, num_phys_pages=4096), 2),
 ])
 def test_validation(spg, change, status):
     assert spg.spg_validate(_valid(spg, **change)) == status
