@@ -14,6 +14,8 @@ Selectors
   sketch  block score = LSE of dequantised int4 sketch logits over the
           block's tokens ("SALS长序列推理优化", QSI); forced = the tail
           block holding token L_b - 1 (n_sink = 0, n_recent = 1).
+  probe   page score = largest q . k over n_probe uniformly sampled tokens
+          of the page, max over the group ("Day 10·2 sparse top-k", §1-§2).
   all     every page (dense attention baseline).
 """
 
@@ -24,7 +26,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import attention, quest, select, sketch
+from . import attention, probe, quest, select, sketch
 
 
 @dataclass
@@ -38,13 +40,14 @@ class StepParams:
     softmax_scale: float = 0.0  # 0 -> 1/sqrt(head_dim)
     top_p: float = 0.0  # adaptive budget: 0 = off (the fixed budget)
     min_pages: int = 0  # adaptive budget: fewest candidate pages kept
+    n_probe: int = 8  # probe selector: sampled tokens per page
 
     @property
     def tau(self) -> float:
         """Temperature of the page-score softmax of the adaptive budget: the
         sketch block score is already a log attention mass (1); the Quest
         bound is on the unscaled dot product, so it takes the softmax scale."""
-        return 1.0 if self.selector == "sketch" else self.scale
+        return 1.0 if self.selector == "sketch" else self.scale  # Quest and probe: dot products
 
     @property
     def scale(self) -> float:
@@ -120,11 +123,31 @@ def unit_sketch_scores(inp: StepInputs, prm: StepParams, b: int, h: int) -> np.n
     return out
 
 
+def unit_probe_scores(inp: StepInputs, prm: StepParams, b: int, h: int) -> np.ndarray:
+    """Probe scores of all pages [0, P_b) of unit (b, h) (forced pages included)."""
+    L = int(inp.seq_lens[b])
+    P = quest.num_pages(L, prm.page_size)
+    q_rows = np.asarray(_group_rows(inp, b, h)).astype(np.float64)
+    out = np.empty(P)
+    for p in range(P):
+        phys = int(inp.page_table[b][p])
+        if inp.k_scale is not None:
+            keys = np.asarray(inp.k_pool[phys, h]).astype(np.float64) * \
+                np.asarray(inp.k_scale[phys, h]).astype(np.float64)[:, None]
+        else:
+            keys = np.asarray(inp.k_pool[phys, h]).astype(np.float64)
+        pos = probe.probe_positions(p, prm.page_size, L, prm.n_probe)
+        out[p] = probe.probe_score(q_rows, keys, pos, p * prm.page_size)
+    return out
+
+
 def unit_scores(inp: StepInputs, prm: StepParams, b: int, h: int) -> np.ndarray:
     if prm.selector == "quest":
         return unit_quest_scores(inp, prm, b, h)
     if prm.selector == "sketch":
         return unit_sketch_scores(inp, prm, b, h)
+    if prm.selector == "probe":
+        return unit_probe_scores(inp, prm, b, h)
     raise ValueError(prm.selector)
 
 
