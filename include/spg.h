@@ -98,7 +98,8 @@ typedef enum {
 typedef enum {
   SPG_SEL_QUEST = 0,       /* per-page per-channel min/max upper bound */
   SPG_SEL_SKETCH_INT4 = 1, /* int4 low-rank index key, block log-sum-exp */
-  SPG_SEL_ALL = 2          /* every page (dense attention) */
+  SPG_SEL_ALL = 2,         /* every page (dense attention) */
+  SPG_SEL_PROBE = 3        /* largest q.k over a few sampled keys of each page */
 } spg_selector;
 
 typedef enum { SPG_F16 = 0, SPG_BF16 = 1, SPG_I8 = 2 } spg_dtype;
@@ -141,6 +142,13 @@ typedef struct spg_params {
    * Needs n_sel <= 1024 (SPG_EUNSUPPORTED beyond); ignored by SPG_SEL_ALL. */
   float top_p;
   int32_t min_pages;         /* adaptive budget: fewest candidate pages kept (>= 0) */
+  /* Probe selector (Day 10·2 sparse top-k, §1-§2): a page's score is the
+   * largest q . k (max also over the group's query heads) over n_probe of
+   * its tokens, sampled from its first token in steps of max(valid tokens /
+   * n_probe, 1).  0 => 8.  The probe selector has no metadata: it reads the
+   * keys, so the `minmax` argument of every entry point is the K pool for it
+   * (and sparse_page_meta_update has nothing to do).  fp16/bf16 pools only. */
+  int32_t n_probe;
 } spg_params;
 
 /* Library ABI version (SPG_ABI_VERSION of the build). */

@@ -17,12 +17,12 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspg.so")
 
 SPG_OK, SPG_EINVAL, SPG_EUNSUPPORTED, SPG_ECUDA, SPG_EWORKSPACE = 0, 1, 2, 3, 4
-SEL_QUEST, SEL_SKETCH_INT4, SEL_ALL = 0, 1, 2
+SEL_QUEST, SEL_SKETCH_INT4, SEL_ALL, SEL_PROBE = 0, 1, 2, 3
 F16, BF16, I8 = 0, 1, 2
 DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_SEL, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 _DTYPES = {"f16": F16, "bf16": BF16, "i8": I8}
-_SELECTORS = {"quest": SEL_QUEST, "sketch": SEL_SKETCH_INT4, "all": SEL_ALL}
+_SELECTORS = {"quest": SEL_QUEST, "sketch": SEL_SKETCH_INT4, "all": SEL_ALL, "probe": SEL_PROBE}
 
 
 class SpgError(RuntimeError):
@@ -50,6 +50,7 @@ class spg_params(ctypes.Structure):
         ("softmax_scale", c_float),
         ("top_p", c_float),
         ("min_pages", c_int32),
+        ("n_probe", c_int32),
     ]
 
     def __repr__(self):
@@ -59,7 +60,7 @@ class spg_params(ctypes.Structure):
 def make_params(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_phys_pages,
                 max_pages_per_seq, kv_dtype="f16", q_dtype=None, selector="quest",
                 token_budget=0, n_sink_pages=0, n_recent_pages=0, sketch_dim=16,
-                softmax_scale=0.0, top_p=0.0, min_pages=0) -> spg_params:
+                softmax_scale=0.0, top_p=0.0, min_pages=0, n_probe=0) -> spg_params:
     kv = _DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
     if q_dtype is None:
         q_dtype = kv if kv != I8 else F16
@@ -67,7 +68,7 @@ def make_params(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_phys_
     sel = _SELECTORS[selector] if isinstance(selector, str) else int(selector)
     return spg_params(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_phys_pages,
                       max_pages_per_seq, kv, qd, sel, token_budget, n_sink_pages, n_recent_pages,
-                      sketch_dim, softmax_scale, top_p, min_pages)
+                      sketch_dim, softmax_scale, top_p, min_pages, n_probe)
 
 
 def _load():

@@ -102,7 +102,9 @@ spg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SPG_OK : SPG_E
 // the selector's metadata inputs
 spg_status check_meta_inputs(const spg_params* p, const void* minmax, const uint8_t* sketch,
                              const float* sketch_scale, const float* proj) {
-  if (p->selector == SPG_SEL_QUEST) return ok_ptr(minmax) ? SPG_OK : SPG_EINVAL;
+  // (the probe selector's "metadata" is the K pool itself)
+  if (p->selector == SPG_SEL_QUEST || p->selector == SPG_SEL_PROBE)
+    return ok_ptr(minmax) ? SPG_OK : SPG_EINVAL;
   if (p->selector == SPG_SEL_SKETCH_INT4)
     return (ok_ptr(sketch) && ok_ptr(sketch_scale) && ok_ptr(proj)) ? SPG_OK : SPG_EINVAL;
   return SPG_EINVAL;  // SPG_SEL_ALL has no metadata and no selection
@@ -142,7 +144,7 @@ cudaError_t select_attend(const spg_params& p, const void* q, const void* k_pool
                                             sel_cnt, out, lse, append, w, st);
     if (e != cudaErrorNotSupported) return e;
   }
-  if (append) {
+  if (append && p.selector != SPG_SEL_PROBE) {  // the probe selector keeps no metadata
     const cudaError_t e = spg::launch_meta_update(p, k_pool, k_scale, page_table, seq_lens, 0,
                                                   minmax, const_cast<uint8_t*>(sketch),
                                                   const_cast<float*>(sketch_scale), proj, w.err,
@@ -196,7 +198,8 @@ spg_status spg_validate(const spg_params* p) {
   if (p->kv_dtype < SPG_F16 || p->kv_dtype > SPG_I8) return SPG_EINVAL;
   if (p->q_dtype != SPG_F16 && p->q_dtype != SPG_BF16) return SPG_EINVAL;
   if (p->kv_dtype != SPG_I8 && p->q_dtype != p->kv_dtype) return SPG_EINVAL;
-  if (p->selector < SPG_SEL_QUEST || p->selector > SPG_SEL_ALL) return SPG_EINVAL;
+  if (p->selector < SPG_SEL_QUEST || p->selector > SPG_SEL_PROBE) return SPG_EINVAL;
+  if (p->n_probe < 0) return SPG_EINVAL;
   if (!(p->softmax_scale >= 0.f) || std::isinf(p->softmax_scale)) return SPG_EINVAL;
   if (!(p->top_p >= 0.f && p->top_p <= 1.f) || p->min_pages < 0) return SPG_EINVAL;
   if (p->selector != SPG_SEL_ALL) {
@@ -213,6 +216,7 @@ spg_status spg_validate(const spg_params* p) {
   if (p->head_dim != 64 && p->head_dim != 128) return SPG_EUNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8) return SPG_EUNSUPPORTED;
   if (p->selector == SPG_SEL_QUEST && p->kv_dtype == SPG_I8) return SPG_EUNSUPPORTED;
+  if (p->selector == SPG_SEL_PROBE && p->kv_dtype == SPG_I8) return SPG_EUNSUPPORTED;
   // the tensor-core consumers take 16-token tiles of a staged page, and a
   // ring of four stages must hold four pages (K, V and int8 scales)
   if (p->page_size < 16) return SPG_EUNSUPPORTED;
@@ -252,6 +256,7 @@ spg_status sparse_page_meta_update(const spg_params* p, const void* k_pool, cons
   if ((s = check_meta_inputs(p, minmax, sketch, sketch_scale, proj)) != SPG_OK) return s;
   if ((s = check_ws(p, ws, ws_bytes)) != SPG_OK) return s;
   const Workspace w = spg::carve_workspace(*p, ws);
+  if (p->selector == SPG_SEL_PROBE) return SPG_OK;  // no metadata to keep
   return cuda_status(spg::launch_meta_update(*p, k_pool, k_scale, page_table, seq_lens, rebuild,
                                              minmax, sketch, sketch_scale, proj, w.err,
                                              reinterpret_cast<cudaStream_t>(stream)));
@@ -348,7 +353,7 @@ spg_status sparse_decode_step(const spg_params* p, const void* q, const void* k_
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   int append_inside = (use_sched(*p, 1) || use_fused(*p, 1)) ? 1 : 0;
-  if (!append_inside)
+  if (!append_inside && p->selector != SPG_SEL_PROBE)
     e = spg::launch_meta_update(*p, k_pool, k_scale, page_table, seq_lens, 0, minmax, sketch,
                                 sketch_scale, proj, w.err, st);
   if (e == cudaSuccess)
@@ -395,6 +400,7 @@ const char* spg_step_kernel(const spg_params* p) {
   if (p->selector == SPG_SEL_ALL) return "k_attn";
   if (use_fused(*p, 1)) return "k_fused";
   if (use_sched(*p, 1)) return "k_sched";
+  if (p->selector == SPG_SEL_PROBE) return "k_probe_select+k_attn";
   return p->selector == SPG_SEL_QUEST ? "k_quest_select+k_attn" : "k_sketch_select+k_attn";
 }
 
@@ -402,8 +408,9 @@ int32_t spg_step_launches(const spg_params* p) {
   if (spg_validate(p) != SPG_OK) return 0;
   if (p->selector == SPG_SEL_ALL) return 1;
   if (use_sched(*p, 1) || use_fused(*p, 1)) return 1;
-  // append, scoring (+ a separate selection kernel past 8192 pages), attention
-  return p->max_pages_per_seq > 8192 ? 4 : 3;
+  // append (none for the probe selector), scoring (+ a separate selection
+  // kernel past 8192 pages), attention
+  return (p->selector == SPG_SEL_PROBE ? 2 : 3) + (p->max_pages_per_seq > 8192 ? 1 : 0);
 }
 
 spg_status spg_set_step_kernel(int32_t kernel) {

@@ -20,6 +20,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 128;  // split-K partials per (batch, q-head) held in the workspace
 constexpr int kMaxTopkPages = 49152;  // candidate keys of one (batch, kv-head) kept in shared memory
 constexpr int kMaxTopPPages = 1024;   // largest page budget of the adaptive (top-p) selection
+constexpr int kDefaultProbes = 8;     // probe selector: sampled tokens per page when n_probe is 0
 
 // ---- element conversions -------------------------------------------------
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }

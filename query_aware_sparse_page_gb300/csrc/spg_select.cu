@@ -37,6 +37,7 @@ constexpr int kFusedTopkMaxPages = 8192;
 
 struct SelectArgs {
   const void* q;
+  const void* k_pool;  // probe selector: the keys it samples
   const int32_t* page_table;
   const int32_t* seq_lens;
   const void* minmax;
@@ -52,6 +53,7 @@ struct SelectArgs {
   float inv_sqrt_d;
   float top_p, tau;  // adaptive budget (top_p 0: off)
   int min_pages;
+  int n_probe;       // probe selector: sampled tokens per page
 };
 
 // Selection of one unit from its scores row (global, written by this launch
@@ -222,6 +224,78 @@ __global__ void __launch_bounds__(256) k_sketch_select(const SelectArgs a, int f
   if (fused) arrive_and_select(a, unit, P, lo, hi, s_keys, s_t, &s_last, reinterpret_cast<uint32_t*>(s_P));
 }
 
+// Probe scores (+ fused selection; Day 10·2 sparse top-k, §1-§2): grid
+// (ceil(MP / 32), B*Hkv), 128 threads, one warp per page at a time (8 pages
+// per warp).  A page's score is the largest q . k over its sampled tokens:
+// from the page's first token in steps of max(valid / n_probe, 1), the max
+// also over the group's G query rows.  Each sampled key row (d elements,
+// contiguous) is one coalesced warp load; a warp keeps up to 8 rows in
+// flight; q in registers (d / 32 channels per lane, fp32); dot products
+// summed over the warp by shuffles.
+constexpr int kProbePagesPerCta = 32;
+constexpr int kProbeMaxInFlight = 8;
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) k_probe_select(const SelectArgs a, int fused) {
+  constexpr int CPL = D / 32;  // channels per lane
+  extern __shared__ __align__(128) uint32_t s_keys[];
+  __shared__ TopkShared s_t;
+  __shared__ int s_last;
+  __shared__ __align__(16) uint32_t s_scratch[kTopPScratchWords + 80];
+  pdl_wait();
+  const int unit = blockIdx.y, Hkv = a.Hkv, S = a.S;
+  const int b = unit / Hkv, h = unit % Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int L;
+  const int P = seq_pages(a, b, &L);
+  const int lo = min(a.n_sink, P), hi = max(P - a.n_recent, lo);
+  float qf[G][CPL];
+  const T* qb = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hkv * G + h * G) * D;
+#pragma unroll
+  for (int g = 0; g < G; ++g) load_cvt<T, CPL>(qb + g * D + lane * CPL, qf[g]);
+  const int n_probe = max(a.n_probe, 1);
+  for (int j = warp; j < kProbePagesPerCta; j += 4) {
+    const int p = blockIdx.x * kProbePagesPerCta + j;
+    if (p >= a.MP) break;
+    float score = -INFINITY;
+    if (p >= lo && p < hi) {  // a candidate page
+      const int phys = a.page_table[static_cast<size_t>(b) * a.MP + p];
+      if (phys < 0 || phys >= a.n_phys) {
+        if (lane == 0) record_error(a.err, SPG_DEVERR_PAGE_ID);
+      } else {
+        const int valid = min(S, L - p * S);
+        const int step = max(valid / n_probe, 1);
+        const T* page = static_cast<const T*>(a.k_pool) + (static_cast<size_t>(phys) * Hkv + h) * S * D;
+        for (int t0 = 0; t0 < valid; t0 += step * kProbeMaxInFlight) {
+          float kf[kProbeMaxInFlight][CPL];
+#pragma unroll
+          for (int r = 0; r < kProbeMaxInFlight; ++r) {
+            const int t = t0 + r * step;
+            if (t < valid) load_cvt<T, CPL>(page + static_cast<size_t>(t) * D + lane * CPL, kf[r]);
+          }
+#pragma unroll
+          for (int r = 0; r < kProbeMaxInFlight; ++r) {
+            const int t = t0 + r * step;
+            if (t < valid) {  // warp-uniform
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                float acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc = fmaf(qf[g][c], kf[r][c], acc);
+                acc = warp_sum(acc);
+                score = fmaxf(score, acc);
+              }
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) a.scores[static_cast<size_t>(unit) * a.MP + p] = score;
+  }
+  pdl_trigger();
+  if (fused) arrive_and_select(a, unit, P, lo, hi, s_keys, s_t, &s_last, s_scratch);
+}
+
 // Selection alone, for page tables too long to select inside the scoring
 // launch: one CTA (1024 threads) per (batch, kv-head).
 __global__ void __launch_bounds__(1024) k_topk(const SelectArgs a) {
@@ -288,6 +362,25 @@ __global__ void __launch_bounds__(256) k_sketch_dots(const SelectArgs a, int32_t
 }
 
 template <typename T>
+cudaError_t probe_typed(const spg_params& p, const SelectArgs& a, int fused, size_t smem_keys,
+                        cudaStream_t st) {
+  dim3 grid((p.max_pages_per_seq + kProbePagesPerCta - 1) / kProbePagesPerCta,
+            p.batch * p.num_kv_heads);
+  const int G = a.G;
+#define SPG_PS(D_, G_)                                          \
+  if (p.head_dim == D_ && G == G_) {                             \
+    auto kern = k_probe_select<T, D_, G_>;                       \
+    cudaError_t e = ensure_smem(kern, smem_keys);                \
+    if (e != cudaSuccess) return e;                              \
+    return launch_pdl(kern, grid, dim3(128), smem_keys, st, a, fused); \
+  }
+  SPG_PS(128, 1) SPG_PS(128, 2) SPG_PS(128, 4) SPG_PS(128, 8)
+  SPG_PS(64, 1) SPG_PS(64, 2) SPG_PS(64, 4) SPG_PS(64, 8)
+#undef SPG_PS
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
 cudaError_t quest_typed(const spg_params& p, const SelectArgs& a, int fused, size_t smem_keys,
                         cudaStream_t st) {
   dim3 grid((p.max_pages_per_seq + kQuestPagesPerCta - 1) / kQuestPagesPerCta,
@@ -340,12 +433,17 @@ cudaError_t launch_select(const spg_params& p, const void* q, const int32_t* pag
   a.top_p = p.top_p;
   a.min_pages = p.min_pages;
   a.tau = p.selector == SPG_SEL_SKETCH_INT4
-              ? 1.0f
+              ? 1.0f  // a log block mass; Quest and probe scores are dot products
               : (p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf(static_cast<float>(p.head_dim)));
+  a.n_probe = p.n_probe > 0 ? p.n_probe : kDefaultProbes;
+  a.k_pool = minmax;  // the probe selector samples the keys themselves
   const int fused = (sel != nullptr && p.max_pages_per_seq <= kFusedTopkMaxPages) ? 1 : 0;
   const size_t smem = fused ? sizeof(uint32_t) * p.max_pages_per_seq : 0;
   cudaError_t e;
-  if (p.selector == SPG_SEL_QUEST) {
+  if (p.selector == SPG_SEL_PROBE) {
+    e = p.kv_dtype == SPG_F16 ? probe_typed<__half>(p, a, fused, smem, stream)
+                              : probe_typed<__nv_bfloat16>(p, a, fused, smem, stream);
+  } else if (p.selector == SPG_SEL_QUEST) {
     e = p.kv_dtype == SPG_F16 ? quest_typed<__half>(p, a, fused, smem, stream)
                               : quest_typed<__nv_bfloat16>(p, a, fused, smem, stream);
   } else {
