@@ -41,6 +41,7 @@ class StepParams:
     top_p: float = 0.0  # adaptive budget: 0 = off (the fixed budget)
     min_pages: int = 0  # adaptive budget: fewest candidate pages kept
     n_probe: int = 8  # probe selector: sampled tokens per page
+    meta_dtype: str = "f16"  # Quest over int8 keys: the stored metadata type (the query's)
 
     @property
     def tau(self) -> float:
@@ -87,6 +88,11 @@ def unit_quest_scores(inp: StepInputs, prm: StepParams, b: int, h: int) -> np.nd
         phys = int(inp.page_table[b][p])
         t0, t1 = quest.page_token_range(p, prm.page_size, L)
         keys = np.asarray(inp.k_pool[phys, h, : t1 - t0]).astype(np.float64)
+        if inp.k_scale is not None:  # int8 codes: dequantised, stored rounded outward
+            keys = keys * np.asarray(inp.k_scale[phys, h, : t1 - t0]).astype(np.float64)[:, None]
+            m[p] = quest.round_outward(keys.min(axis=0), prm.meta_dtype, down=True)
+            M[p] = quest.round_outward(keys.max(axis=0), prm.meta_dtype, down=False)
+            continue
         m[p] = keys.min(axis=0)
         M[p] = keys.max(axis=0)
     q_rows = np.asarray(_group_rows(inp, b, h)).astype(np.float64)

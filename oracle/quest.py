@@ -8,6 +8,13 @@ attention time).  GQA handling follows the same page's "GQA 下的并集放大"
 section: one selection shared by the query heads of a kv-head group; the
 group score is the largest per-head bound, so the bound still holds for
 every query head of the group.
+
+Quantised keys (the same page, 与量化、GQA、多页并行的兼容性: the min/max
+metadata can be taken from the quantised KV directly): for int8 codes with a
+per-token fp16 scale, m and M are the min and max of the dequantised keys
+code * scale (exact in fp32), stored in a 16-bit type rounded outward (m
+down, M up), so that the stored interval still contains every key and the
+bound stays an upper bound (page_minmax_dequant).
 """
 
 from __future__ import annotations
@@ -73,3 +80,41 @@ def group_scores(q_group, m, M):
     """
     per_head = np.stack([head_bound(qh, m, M) for qh in np.asarray(q_group, dtype=np.float64)])
     return per_head.max(axis=0)
+
+
+def round_outward(x, dtype: str, down: bool):
+    """x (values exact in fp32) rounded toward -inf (down) or +inf (up) to
+    the 16-bit type dtype ("f16" or "bf16"), returned as fp64."""
+    x = np.asarray(x, dtype=np.float32)
+    if dtype == "f16":
+        y = x.astype(np.float16)  # round to nearest
+        if down:
+            y = np.where(y.astype(np.float32) > x, np.nextafter(y, np.float16(-np.inf)), y)
+        else:
+            y = np.where(y.astype(np.float32) < x, np.nextafter(y, np.float16(np.inf)), y)
+        return y.astype(np.float64)
+    # bf16: the upper half of the fp32 bit pattern; cutting the low half
+    # rounds toward zero, one step of the kept half away from zero fixes the
+    # other direction
+    u = x.view(np.uint32)
+    t = u & np.uint32(0xFFFF0000)
+    v = t.view(np.float32)
+    bump = (v > x) if down else (v < x)
+    t = np.where(bump, t + np.uint32(0x10000), t)
+    return t.view(np.float32).astype(np.float64)
+
+
+def page_minmax_dequant(codes, scales, page_table, seq_lens, page_size, meta_dtype):
+    """Quest metadata of int8 keys with per-token scales, as stored.
+
+    codes: [P_phys][Hkv][S][d] int8; scales: [P_phys][Hkv][S] fp16.
+    Returns fp64 [P_phys][Hkv][2][d] (m rounded down, M rounded up to
+    meta_dtype), NaN in unused pages.
+    """
+    deq = np.asarray(codes).astype(np.float64) * np.asarray(scales).astype(np.float64)[..., None]
+    exact = page_minmax(deq, page_table, seq_lens, page_size)
+    out = exact.copy()
+    used = ~np.isnan(exact[:, :, 0, 0])
+    out[used, 0] = round_outward(exact[used, 0], meta_dtype, down=True)
+    out[used, 1] = round_outward(exact[used, 1], meta_dtype, down=False)
+    return out

@@ -114,3 +114,59 @@ def test_planted_mistake_is_caught(rng, monkeypatch):
     monkeypatch.setattr(quest, "head_bound", swapped)
     with pytest.raises(AssertionError):
         test_bound_equals_box_corner_maximum(rng)
+
+
+# ---- Quest over int8 keys (与量化、GQA、多页并行的兼容性) ---------------------
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_round_outward_brackets_within_one_step(rng, dtype):
+    import torch
+
+    x = (rng.standard_normal(4000) * rng.choice([0.01, 1.0, 300.0], 4000)).astype(np.float32)
+    lo = quest.round_outward(x, dtype, down=True)
+    hi = quest.round_outward(x, dtype, down=False)
+    assert np.all(lo <= x) and np.all(hi >= x)
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    # both ends are values of the 16-bit type, next to each other (or equal when x is one)
+    for v in (lo, hi):
+        back = torch.tensor(v, dtype=torch.float64).to(tdt).to(torch.float64).numpy()
+        assert np.array_equal(back, v)
+    exact = torch.tensor(x).to(tdt).to(torch.float32).numpy() == x
+    assert np.all((lo == hi) == exact)
+    nxt = torch.nextafter(torch.tensor(lo, dtype=torch.float32).to(tdt) if dtype == "f16" else
+                          torch.tensor(lo, dtype=torch.float32).to(tdt),
+                          torch.full(x.shape, float("inf")).to(tdt))
+    assert np.all((hi == lo) | (hi == nxt.to(torch.float64).numpy()))
+
+
+def test_dequant_metadata_bounds_every_dequantised_key(rng):
+    """The bound over int8 keys with per-token scales stays an upper bound of
+    q . k for every token of every page (the Quest invariant), and the stored
+    interval is at most one step of the stored type wider than the exact one."""
+    P_phys, Hkv, S, d = 9, 2, 16, 32
+    codes = rng.integers(-127, 128, (P_phys, Hkv, S, d)).astype(np.int8)
+    scales = (rng.random((P_phys, Hkv, S)) * 0.05 + 0.001).astype(np.float16)
+    pt = np.array([[3, 1, 4, 0, 8, 2, 7, 5, 6]])
+    L = 8 * S + 5
+    for meta in ("f16", "bf16"):
+        mm = quest.page_minmax_dequant(codes, scales, pt, [L], S, meta)
+        deq = codes.astype(np.float64) * scales.astype(np.float64)[..., None]
+        exact = quest.page_minmax(deq, pt, [L], S)
+        used = ~np.isnan(exact[:, 0, 0, 0])
+        assert np.all(mm[used, :, 0] <= exact[used, :, 0]) and np.all(mm[used, :, 1] >= exact[used, :, 1])
+        q = rng.standard_normal((2, d))
+        for p in range(9):
+            phys = pt[0, p]
+            n = min(S, L - p * S)
+            for h in range(Hkv):
+                bound = quest.group_scores(q, mm[phys, h, 0][None], mm[phys, h, 1][None])[0]
+                assert bound >= (q @ deq[phys, h, :n].T).max() - 1e-12
+
+
+def test_dequant_metadata_is_exact_when_representable():
+    # unit scales and small codes: every key is a 16-bit value, nothing rounds
+    codes = np.arange(-8, 8, dtype=np.int8).reshape(1, 1, 2, 8)
+    scales = np.ones((1, 1, 2), np.float16)
+    mm = quest.page_minmax_dequant(codes, scales, np.array([[0]]), [2], 2, "f16")
+    assert np.array_equal(mm[0, 0, 0], np.minimum(codes[0, 0, 0], codes[0, 0, 1]).astype(np.float64))
+    assert np.array_equal(mm[0, 0, 1], np.maximum(codes[0, 0, 0], codes[0, 0, 1]).astype(np.float64))
