@@ -48,10 +48,14 @@
  *   page_table   [B][MP] int32         physical page of each logical page
  *   seq_lens     [B] int32             tokens in each sequence, counting the
  *                                      token appended this step
- *   minmax       [B][Hkv][MP][2][d]    kv_dtype; per sequence, kv-head and
- *                                      LOGICAL page: [..][0][:] = per-channel
- *                                      min m, [..][1][:] = max M of K over
- *                                      the page's valid tokens (Quest)
+ *   minmax       [B][Hkv][MP][2][d]    kv_dtype (q_dtype for int8 pools);
+ *                                      per sequence, kv-head and LOGICAL
+ *                                      page: [..][0][:] = per-channel min m,
+ *                                      [..][1][:] = max M of K over the
+ *                                      page's valid tokens (Quest); for int8
+ *                                      pools the min / max of the dequantised
+ *                                      keys code * scale, rounded outward (m
+ *                                      down, M up) to the 16-bit type
  *   sketch       [B][Hkv][MP][S][ds/2] uint8, per logical block; int4 codes
  *                                      of the projected keys, two's
  *                                      complement, channel 2j in the low

@@ -34,7 +34,9 @@ def alloc_buffers(p, device="cuda") -> DecodeBuffers:
     n_sel = max(p.token_budget // S, 1)
     minmax = sketch = sketch_scale = None
     if p.selector == SEL_QUEST:
-        minmax = torch.zeros((B, Hkv, MP, 2, d), dtype=_TORCH_KV[p.kv_dtype], device=dev)
+        # int8 pools keep their Quest metadata in the query's 16-bit type
+        mdt = _TORCH_KV[p.q_dtype] if p.kv_dtype == I8 else _TORCH_KV[p.kv_dtype]
+        minmax = torch.zeros((B, Hkv, MP, 2, d), dtype=mdt, device=dev)
     elif p.selector == SEL_SKETCH_INT4:
         sketch = torch.zeros((B, Hkv, MP, S, p.sketch_dim // 2), dtype=torch.uint8, device=dev)
         sketch_scale = torch.zeros((B, Hkv, MP), dtype=torch.float32, device=dev)

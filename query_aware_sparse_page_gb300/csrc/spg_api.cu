@@ -215,7 +215,6 @@ spg_status spg_validate(const spg_params* p) {
   const int G = p->num_q_heads / p->num_kv_heads;
   if (p->head_dim != 64 && p->head_dim != 128) return SPG_EUNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8) return SPG_EUNSUPPORTED;
-  if (p->selector == SPG_SEL_QUEST && p->kv_dtype == SPG_I8) return SPG_EUNSUPPORTED;
   if (p->selector == SPG_SEL_PROBE && p->kv_dtype == SPG_I8) return SPG_EUNSUPPORTED;
   // the tensor-core consumers take 16-token tiles of a staged page, and a
   // ring of four stages must hold four pages (K, V and int8 scales)

@@ -45,6 +45,54 @@ __device__ void minmax_append_warp(const T* k_pool, const int32_t* page_table, T
   }
 }
 
+// fp32 -> 16-bit type rounded toward -inf / +inf (the Quest interval of
+// int8 keys is stored rounded outward, so it still holds every key)
+template <typename TM> __device__ __forceinline__ TM round_down16(float x);
+template <typename TM> __device__ __forceinline__ TM round_up16(float x);
+template <> __device__ __forceinline__ __half round_down16<__half>(float x) { return __float2half_rd(x); }
+template <> __device__ __forceinline__ __half round_up16<__half>(float x) { return __float2half_ru(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 round_down16<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rd(x);
+}
+template <> __device__ __forceinline__ __nv_bfloat16 round_up16<__nv_bfloat16>(float x) {
+  return __float2bfloat16_ru(x);
+}
+
+// Quest append of token L-1 of (b, h) over an int8 pool with per-token fp16
+// scales (Quest 完全拆解, 与量化的兼容性: the metadata taken from the
+// quantised keys): the dequantised key code * scale (exact in fp32) widens
+// the page's interval, stored in TM rounded outward.  One warp.
+template <typename TM, int D>
+__device__ void minmax_append_warp_i8(const int8_t* k_pool, const __half* k_scale,
+                                      const int32_t* page_table, TM* minmax, int32_t* err, int Hkv,
+                                      int S, int MP, int n_phys, int b, int h, int L, int lane) {
+  constexpr int CPL = D / 32;
+  const int t = L - 1, p = t / S, slot = t % S;
+  const int phys = page_table[static_cast<size_t>(b) * MP + p];
+  if (phys < 0 || phys >= n_phys) {
+    if (lane == 0) record_error(err, SPG_DEVERR_PAGE_ID);
+    return;
+  }
+  const size_t ph = static_cast<size_t>(phys) * Hkv + h;
+  const int8_t* k = k_pool + (ph * S + slot) * D + lane * CPL;
+  const float sc = __half2float(k_scale[ph * S + slot]);
+  TM* row = minmax + ((static_cast<size_t>(b) * Hkv + h) * MP + p) * 2 * D;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const float v = __fmul_rn(static_cast<float>(k[c]), sc);
+    const TM dn = round_down16<TM>(v), up = round_up16<TM>(v);
+    TM& lo = row[meta_swz<TM>(lane * CPL + c, p)];
+    TM& hi = row[meta_swz<TM>(D + lane * CPL + c, p)];
+    if (slot == 0) {
+      lo = dn;
+      hi = up;
+    } else {
+      if (to_f32(dn) < to_f32(lo)) lo = dn;
+      if (to_f32(up) > to_f32(hi)) hi = up;
+    }
+  }
+}
+
 // 16 consecutive channels of a key row as fp32 (row 16-byte aligned)
 template <typename T>
 __device__ __forceinline__ void load16_f32(const T* p, float (&x)[16]) {

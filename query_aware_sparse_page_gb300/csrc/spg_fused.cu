@@ -182,6 +182,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   // pages (D = 128, fp16 query), 0 = CUDA cores; 1 and 2 take TMA tiles
   constexpr int CONS = !is_i8<T>() ? 1 : ((D == 128 && std::is_same<TQ, __half>::value) ? 2 : 0);
   constexpr bool MMA = CONS != 0;
+  // Quest metadata type: the pool's, or the query's for int8 pools
+  using TM = std::conditional_t<is_i8<T>(), TQ, T>;
   const int C = a.cluster;
   using Consumer = std::conditional_t<
       CONS == 1, AttnMma<T, D, G>,
@@ -307,9 +309,16 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       mbar_arrive(&s_ptbar);
     }
     if constexpr (SEL == 0) {
-      if (a.append && rank == C - 1 && L > 0)
-        minmax_append_warp<T, D>(static_cast<const T*>(a.k_pool), a.page_table, static_cast<T*>(a.minmax),
-                                 a.err, a.Hkv, a.S, a.MP, a.n_phys, b, h, L, lane);
+      if (a.append && rank == C - 1 && L > 0) {
+        if constexpr (is_i8<T>())
+          minmax_append_warp_i8<TM, D>(static_cast<const int8_t*>(a.k_pool), a.k_scale, a.page_table,
+                                       static_cast<TM*>(a.minmax), a.err, a.Hkv, a.S, a.MP, a.n_phys,
+                                       b, h, L, lane);
+        else
+          minmax_append_warp<T, D>(static_cast<const T*>(a.k_pool), a.page_table,
+                                   static_cast<T*>(a.minmax), a.err, a.Hkv, a.S, a.MP, a.n_phys, b, h,
+                                   L, lane);
+      }
     } else {
       // the sketch of a block is written when the block fills (every CTA's
       // aux warp takes a slice)
@@ -320,8 +329,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     // consumers
     uint32_t kmn = 0xffffffffu, kmx = 0u;  // of the keys this warp produces
     if constexpr (SEL == 0) {
-      QuestMma<T, D, G> qm;
-      qm.init(static_cast<const T*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D, lane);
+      QuestMma<TM, D, G> qm;
+      qm.init(static_cast<const TM*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D, lane);
       for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
         if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
@@ -330,7 +339,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
           break;
         }
         const int nr = min(R, rows - ks * R);
-        const T* st = reinterpret_cast<const T*>(ring + static_cast<size_t>(stage) * sbytes);
+        const TM* st = reinterpret_cast<const TM*>(ring + static_cast<size_t>(stage) * sbytes);
         for (int ti = 0; ti * 16 < nr; ++ti) {  // the stage's 16-page tiles
           const int pt0 = c0 + ks * R + ti * 16;
           float s0, s1;
@@ -628,7 +637,8 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   constexpr bool MMA = !is_i8<T>() || (D == 128 && std::is_same<TQ, __half>::value);
   // a page's K tile must start 1024-byte aligned for the swizzled TMA tiles
   const uint32_t pb = MMA ? (kv_stage_bytes<T, D>(S) + 1023u) & ~1023u : kv_stage_bytes<T, D>(S);
-  const uint32_t rb = p.selector == SPG_SEL_QUEST ? 2u * D * sizeof(T) : static_cast<uint32_t>(S) * 8u;
+  using TM = std::conditional_t<is_i8<T>(), TQ, T>;  // Quest metadata type
+  const uint32_t rb = p.selector == SPG_SEL_QUEST ? 2u * D * sizeof(TM) : static_cast<uint32_t>(S) * 8u;
   int pps = 1;
   while (pps * 2 <= kMaxPagesPerStage && (pps * 2) * pb <= static_cast<uint32_t>(kStageBytesTarget))
     pps *= 2;
@@ -677,9 +687,7 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   a.sel_off = static_cast<uint32_t>(sel_off);
   a.att_off = static_cast<uint32_t>(att_off);
 
-  auto kern = k_fused<T, TQ, D, G, 1>;  // int8 pools are only scored by the sketch selector
-  if constexpr (!is_i8<T>())
-    if (p.selector == SPG_SEL_QUEST) kern = k_fused<T, TQ, D, G, 0>;
+  auto kern = p.selector == SPG_SEL_QUEST ? k_fused<T, TQ, D, G, 0> : k_fused<T, TQ, D, G, 1>;
   cudaError_t e = ensure_smem(kern, smem);
   if (e != cudaSuccess) return e;
   // cluster size: 8 CTAs per unit when the GPU can hold them all at once,

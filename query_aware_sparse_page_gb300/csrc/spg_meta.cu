@@ -16,6 +16,7 @@
 // one rounded add per step, channels in order: the codes are defined by this
 // arithmetic) and quantised to int4 in [-7, 7] with one scale max|k~|/7.
 // The open tail block is never scored, so it is quantised only once full.
+#include "spg_append.cuh"
 #include "spg_common.cuh"
 #include "spg_internal.h"
 
@@ -118,6 +119,96 @@ __global__ void k_minmax_rebuild(const T* __restrict__ k_pool, const int32_t* __
   }
 }
 
+// Quest over int8 keys with per-token fp16 scales (Quest 完全拆解,
+// 与量化的兼容性): the interval of the dequantised keys code * scale (exact in
+// fp32), stored in the query's 16-bit type TM rounded outward.
+// Append: one warp per (batch, kv-head).
+template <typename TM, int D>
+__global__ void k_minmax_append_i8(const int8_t* __restrict__ k_pool, const __half* __restrict__ k_scale,
+                                   const int32_t* __restrict__ page_table,
+                                   const int32_t* __restrict__ seq_lens, TM* __restrict__ minmax,
+                                   int B, int Hkv, int S, int MP, int n_phys, int32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_trigger();
+  const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (unit >= B * Hkv) return;
+  const int b = unit / Hkv, h = unit % Hkv;
+  const int L = seq_lens[b];
+  if (L <= 0 || L > MP * S) {
+    if (L != 0 && lane == 0) record_error(err, SPG_DEVERR_SEQ_LEN);
+    return;
+  }
+  minmax_append_warp_i8<TM, D>(k_pool, k_scale, page_table, minmax, err, Hkv, S, MP, n_phys, b, h, L,
+                               lane);
+}
+
+// Rebuild: one warp per (batch, kv-head, page); fp32 min / max over the
+// page's valid tokens, then one outward rounding each.
+template <typename TM>
+__global__ void k_minmax_rebuild_i8(const int8_t* __restrict__ k_pool, const __half* __restrict__ k_scale,
+                                    const int32_t* __restrict__ page_table,
+                                    const int32_t* __restrict__ seq_lens, TM* __restrict__ minmax,
+                                    int B, int Hkv, int S, int d, int MP, int n_phys,
+                                    int32_t* __restrict__ err) {
+  const int warps_per_block = blockDim.x >> 5;
+  const int p = blockIdx.x * warps_per_block + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.y;
+  const int b = unit / Hkv, h = unit % Hkv;
+  const int L = seq_lens[b];
+  if (L < 0 || L > MP * S) {
+    if (p == 0 && lane == 0) record_error(err, SPG_DEVERR_SEQ_LEN);
+    return;
+  }
+  const int P = (L + S - 1) / S;
+  if (p >= P) return;
+  const int phys = page_table[(size_t)b * MP + p];
+  if (phys < 0 || phys >= n_phys) {
+    if (lane == 0) record_error(err, SPG_DEVERR_PAGE_ID);
+    return;
+  }
+  const int n_valid = min(S, L - p * S);
+  const size_t ph = (size_t)phys * Hkv + h;
+  const int8_t* base = k_pool + ph * S * d;
+  const __half* sc = k_scale + ph * S;
+  TM* mrow = minmax + ((size_t)unit * MP + p) * 2 * d;  // [B][Hkv][MP][2][d]
+  for (int c = lane; c < d; c += 32) {
+    float lo = INFINITY, hi = -INFINITY;
+    for (int t = 0; t < n_valid; ++t) {
+      const float v = __fmul_rn(static_cast<float>(base[(size_t)t * d + c]), __half2float(sc[t]));
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+    mrow[meta_swz<TM>(c, p)] = round_down16<TM>(lo);
+    mrow[meta_swz<TM>(d + c, p)] = round_up16<TM>(hi);
+  }
+}
+
+template <typename TM>
+cudaError_t meta_quest_i8(const spg_params& p, const void* k_pool, const void* k_scale,
+                          const int32_t* pt, const int32_t* lens, int rebuild, void* minmax,
+                          int32_t* err, cudaStream_t st) {
+  const int B = p.batch, Hkv = p.num_kv_heads, S = p.page_size, d = p.head_dim;
+  const int MP = p.max_pages_per_seq, NP = p.num_phys_pages;
+  const int8_t* kp = static_cast<const int8_t*>(k_pool);
+  const __half* ks = static_cast<const __half*>(k_scale);
+  TM* mm = static_cast<TM*>(minmax);
+  if (!rebuild) {
+    const int threads = 128, units = B * Hkv;
+    const int blocks = (units * 32 + threads - 1) / threads;
+    if (d == 128)
+      return launch_pdl(k_minmax_append_i8<TM, 128>, dim3(blocks), dim3(threads), 0, st, kp, ks, pt,
+                        lens, mm, B, Hkv, S, MP, NP, err);
+    return launch_pdl(k_minmax_append_i8<TM, 64>, dim3(blocks), dim3(threads), 0, st, kp, ks, pt, lens,
+                      mm, B, Hkv, S, MP, NP, err);
+  }
+  const int wpb = 8;
+  dim3 grid((MP + wpb - 1) / wpb, B * Hkv);
+  k_minmax_rebuild_i8<TM><<<grid, wpb * 32, 0, st>>>(kp, ks, pt, lens, mm, B, Hkv, S, d, MP, NP, err);
+  return cudaGetLastError();
+}
+
 template <typename T>
 __device__ __forceinline__ float dequant_key(const T* row, const __half* scale, int i) {
   return to_f32(row[i]);
@@ -216,6 +307,11 @@ cudaError_t meta_typed(const spg_params& p, const void* k_pool, const void* k_sc
   const int B = p.batch, Hkv = p.num_kv_heads, S = p.page_size, d = p.head_dim;
   const int MP = p.max_pages_per_seq, NP = p.num_phys_pages;
   const T* kp = static_cast<const T*>(k_pool);
+  if (p.selector == SPG_SEL_QUEST && is_i8<T>()) {
+    return p.q_dtype == SPG_F16
+               ? meta_quest_i8<__half>(p, k_pool, k_scale, pt, lens, rebuild, minmax, err, st)
+               : meta_quest_i8<__nv_bfloat16>(p, k_pool, k_scale, pt, lens, rebuild, minmax, err, st);
+  }
   if (p.selector == SPG_SEL_QUEST) {
     if (!rebuild) {
       const int threads = 128, units = B * Hkv;

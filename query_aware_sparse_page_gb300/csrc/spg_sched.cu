@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
   constexpr int CW = kConsumerWarps;
   constexpr int CONS = !is_i8<T>() ? 1 : ((D == 128 && std::is_same<TQ, __half>::value) ? 2 : 0);
   constexpr bool MMA = CONS != 0;
+  using TM = std::conditional_t<is_i8<T>(), TQ, T>;  // Quest metadata type
   using Consumer = std::conditional_t<
       CONS == 1, AttnMma<T, D, G>,
       std::conditional_t<CONS == 2, AttnMmaI8<G>, AttnConsumer<T, D, G, 1>>>;
@@ -471,10 +472,16 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
       // no scan or attend task of this step reads what is written
       if (a.append && bi.L > 0) {
         if constexpr (SEL == 0) {
-          if (warp == 0)
-            minmax_append_warp<T, D>(static_cast<const T*>(a.k_pool), a.page_table,
-                                     static_cast<T*>(a.minmax), a.err, Hkv, S, MP, a.n_phys, b, h,
-                                     bi.L, lane);
+          if (warp == 0) {
+            if constexpr (is_i8<T>())
+              minmax_append_warp_i8<TM, D>(static_cast<const int8_t*>(a.k_pool), a.k_scale,
+                                           a.page_table, static_cast<TM*>(a.minmax), a.err, Hkv, S,
+                                           MP, a.n_phys, b, h, bi.L, lane);
+            else
+              minmax_append_warp<T, D>(static_cast<const T*>(a.k_pool), a.page_table,
+                                       static_cast<T*>(a.minmax), a.err, Hkv, S, MP, a.n_phys, b,
+                                       h, bi.L, lane);
+          }
         } else {
           if (bi.L % S == 0)
             sketch_block_cta<T, D>(static_cast<const T*>(a.k_pool), a.k_scale, a.page_table, a.proj,
@@ -681,9 +688,9 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
         const int u = d.unit, nr = d.count;
         uint32_t* kout = a.keys + static_cast<size_t>(u) * MP;
         if constexpr (SEL == 0) {
-          QuestMma<T, D, G> qm;
-          qm.init(reinterpret_cast<const T*>(qbuf + static_cast<size_t>(slot) * a.qbytes), lane);
-          const T* st = reinterpret_cast<const T*>(stg);
+          QuestMma<TM, D, G> qm;
+          qm.init(reinterpret_cast<const TM*>(qbuf + static_cast<size_t>(slot) * a.qbytes), lane);
+          const TM* st = reinterpret_cast<const TM*>(stg);
           for (int ti = 0; ti * 16 < nr; ++ti) {
             const int pt0 = d.first + ti * 16;
             float s0, s1;
@@ -830,7 +837,8 @@ cudaError_t sched_typed(const spg_params& p, SchedArgs a, cudaStream_t st) {
   const int n_sel = n_sel_pages(p);
   // a page's K tile starts 1024-byte aligned for the swizzled TMA tiles
   const uint32_t pb = MMA ? (kv_stage_bytes<T, D>(S) + 1023u) & ~1023u : kv_stage_bytes<T, D>(S);
-  const uint32_t rb = SEL == 0 ? 2u * D * sizeof(T) : static_cast<uint32_t>(S) * 8u;
+  using TM = std::conditional_t<is_i8<T>(), TQ, T>;  // Quest metadata type
+  const uint32_t rb = SEL == 0 ? 2u * D * sizeof(TM) : static_cast<uint32_t>(S) * 8u;
   // Two ring slots per consumer warp (8 stages) of about kStageTarget / 2
   // bytes when a page fits in that, else one slot per warp of up to
   // kStageTarget: a warp then has its next stage in flight while it
@@ -960,7 +968,6 @@ cudaError_t sched_dispatch(const spg_params& p, const SchedArgs& a, cudaStream_t
 bool sched_supported(const spg_params& p, int append) {
   if (p.selector != SPG_SEL_QUEST && p.selector != SPG_SEL_SKETCH_INT4) return false;
   if (p.max_pages_per_seq > kSchedMaxPages || p.batch > kSchedMaxBatch) return false;
-  if (p.selector == SPG_SEL_QUEST && p.kv_dtype == SPG_I8) return false;
   if (p.selector == SPG_SEL_SKETCH_INT4 && (p.page_size > 128 || p.sketch_dim != 16)) return false;
   if (append && p.n_recent_pages < 1) return false;  // the appended token's page must be forced
   return true;
@@ -1022,7 +1029,8 @@ cudaError_t launch_sched(const spg_params& p, const void* q, const void* k_pool,
       case SPG_BF16:
         return sched_dispatch<__nv_bfloat16, __nv_bfloat16, 0>(p, a, stream);
       default:
-        return cudaErrorNotSupported;
+        if (p.q_dtype == SPG_F16) return sched_dispatch<int8_t, __half, 0>(p, a, stream);
+        return sched_dispatch<int8_t, __nv_bfloat16, 0>(p, a, stream);
     }
   }
   switch (p.kv_dtype) {

@@ -444,8 +444,10 @@ cudaError_t launch_select(const spg_params& p, const void* q, const int32_t* pag
     e = p.kv_dtype == SPG_F16 ? probe_typed<__half>(p, a, fused, smem, stream)
                               : probe_typed<__nv_bfloat16>(p, a, fused, smem, stream);
   } else if (p.selector == SPG_SEL_QUEST) {
-    e = p.kv_dtype == SPG_F16 ? quest_typed<__half>(p, a, fused, smem, stream)
-                              : quest_typed<__nv_bfloat16>(p, a, fused, smem, stream);
+    // the metadata's type: the pool's, or the query's for int8 pools
+    const int meta = p.kv_dtype == SPG_I8 ? p.q_dtype : p.kv_dtype;
+    e = meta == SPG_F16 ? quest_typed<__half>(p, a, fused, smem, stream)
+                        : quest_typed<__nv_bfloat16>(p, a, fused, smem, stream);
   } else {
     dim3 grid((p.max_pages_per_seq + kSketchBlocksPerCta - 1) / kSketchBlocksPerCta,
               p.batch * p.num_kv_heads);

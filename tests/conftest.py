@@ -42,7 +42,7 @@ def oracle_params(w, selector=None):
 
     return StepParams(
         page_size=w.page_size, n_sel=w.n_sel_pages, n_sink=w.n_sink, n_recent=w.n_recent,
-        selector=selector or w.selector, head_dim=w.head_dim,
+        selector=selector or w.selector, head_dim=w.head_dim, meta_dtype=w.q_dtype,
     )
 
 

@@ -84,6 +84,14 @@ SMALL = {
     "quest-s128-d64": scaled(get_workload("long-scan-b4-128k"), batch=2, num_q_heads=8, num_kv_heads=2,
                              head_dim=64, page_size=128, seq_len=128 * 40 + 77, n_sel_pages=8,
                              needles_per_head=4),
+    # Quest over int8 pools (metadata of the dequantised keys, rounded outward)
+    "quest-i8": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                       page_size=16, seq_len=16 * 150 + 5, selector="quest", n_sel_pages=24,
+                       n_sink=1, n_recent=1),
+    "quest-i8-bf16q-d64": scaled(get_workload("sals-int8-b16-10k-4x"), batch=3, num_q_heads=8,
+                                 num_kv_heads=2, head_dim=64, page_size=32, seq_len=32 * 70 + 19,
+                                 selector="quest", n_sel_pages=12, n_sink=1, n_recent=2,
+                                 q_dtype="bf16"),
 }
 
 
@@ -496,3 +504,38 @@ def test_repeated_steps_on_one_workspace(name):
     finally:
         spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
 
+
+
+@pytest.mark.parametrize("name", ["quest-i8", "quest-i8-bf16q-d64"])
+def test_int8_quest_metadata_bit_exact_and_append_equals_rebuild(name):
+    """Quest over int8 keys: the metadata rebuild equals the oracle's
+    outward-rounded min/max of the dequantised keys bit for bit, and token
+    by token appends give the same rows."""
+    spg = _spg()
+    w = SMALL[name]
+    inp = make_inputs(w, device=DEV)
+    p = spg.params_for(inp)
+    r = spg.alloc_buffers(p, DEV)
+    spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 1,
+                                r.minmax, None, None, None, r.ws)
+    ref = quest.page_minmax_dequant(to_numpy(inp.k_pool), to_numpy(inp.k_scale),
+                                    to_numpy(inp.page_table), to_numpy(inp.seq_lens), w.page_size,
+                                    w.q_dtype)
+    got = to_numpy(r.minmax)
+    pt = to_numpy(inp.page_table)
+    for b, L in enumerate(to_numpy(inp.seq_lens)):
+        for p_ in range(-(-int(L) // w.page_size)):
+            for h in range(w.num_kv_heads):
+                row = unswizzle_meta_row(got[b, h, p_], p_).astype(np.float64)
+                assert np.array_equal(row, ref[pt[b, p_], h]), (b, h, p_)
+    a = spg.alloc_buffers(p, DEV)
+    a.minmax.fill_(3.0)  # stale rows from a recycled page must not leak
+    lens = inp.seq_lens.cpu().tolist()
+    for t in range(1, int(max(lens)) + 1):
+        cur = torch.clamp(torch.tensor(lens, dtype=torch.int32), max=t).to(DEV)
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, cur, 0, a.minmax,
+                                    None, None, None, a.ws)
+    for b, L in enumerate(lens):
+        P = -(-L // w.page_size)
+        assert torch.equal(a.minmax[b, :, :P], r.minmax[b, :, :P])
+    assert spg.spg_read_device_error(a.ws) == 0
