@@ -307,6 +307,19 @@ spg_status sparse_decode_attention_noalloc(const spg_params* p, const void* q, c
                                            const int32_t* sel_cnt, float* out, float* lse,
                                            spg_stream_t stream);
 
+/* Short-sequence dense bypass (Quest 完全拆解, 短序列的负收益: the read ratio
+ * 1/S + K / PageNum has a constant term, so when the sequence is not several
+ * times longer than the token budget the scoring costs more than it saves;
+ * the first-order rule is PageNum at least a few times the K selected
+ * pages).  Host only: returns 1 when a step over sequences of at most
+ * max_seq_len tokens should run dense_decode_attention instead, that is
+ * when ceil(max_seq_len / S) <= ratio * n_sel; ratio <= 0 takes
+ * SPG_DENSE_BYPASS_RATIO, the crossover measured on GB300 for the
+ * benchmark's 32-head MHA (128-page budget) and GQA-8 (256-page budget)
+ * shapes.  0 otherwise, and 0 when spg_validate rejects p or for SPG_SEL_ALL. */
+#define SPG_DENSE_BYPASS_RATIO 2.5f
+int32_t spg_prefer_dense(const spg_params* p, int32_t max_seq_len, float ratio);
+
 /* Which kernel(s) sparse_decode_step launches for these parameters (host
  * only; NULL when spg_validate rejects them): "k_fused" (one thread-block
  * cluster per unit), "k_sched" (the persistent scheduled step), or the

@@ -95,6 +95,7 @@ def _load():
             [P, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
         "sparse_page_sketch_dots": ([P, v, v, v, v, v, v, v, v, c_size_t, v], c_int32),
         "spg_step_kernel": ([P], c_char_p),
+        "spg_prefer_dense": ([P, c_int32, c_float], c_int32),
         "spg_step_launches": ([P], c_int32),
         "spg_set_step_kernel": ([c_int32], c_int32),
         "spg_read_device_error": ([v, POINTER(c_int32), v], c_int32),
@@ -166,6 +167,10 @@ def spg_step_kernel(p: spg_params) -> str | None:
 
 
 step_kernel_name = spg_step_kernel
+
+
+def spg_prefer_dense(p: spg_params, max_seq_len: int, ratio: float = 0.0) -> bool:
+    return bool(LIB.spg_prefer_dense(ctypes.byref(p), int(max_seq_len), float(ratio)))
 
 
 def spg_step_launches(p: spg_params) -> int:

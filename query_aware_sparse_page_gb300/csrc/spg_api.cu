@@ -394,6 +394,13 @@ spg_status sparse_page_sketch_dots(const spg_params* p, const void* q, const int
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int32_t spg_prefer_dense(const spg_params* p, int32_t max_seq_len, float ratio) {
+  if (spg_validate(p) != SPG_OK || p->selector == SPG_SEL_ALL || max_seq_len < 0) return 0;
+  if (!(ratio > 0.f)) ratio = SPG_DENSE_BYPASS_RATIO;
+  const int64_t pages = (static_cast<int64_t>(max_seq_len) + p->page_size - 1) / p->page_size;
+  return static_cast<double>(pages) <= static_cast<double>(ratio) * spg::n_sel_pages(*p) ? 1 : 0;
+}
+
 const char* spg_step_kernel(const spg_params* p) {
   if (spg_validate(p) != SPG_OK) return nullptr;
   if (p->selector == SPG_SEL_ALL) return "k_attn";

@@ -165,3 +165,18 @@ def test_step_kernel_queries(spg):
     assert spg.step_launch_count(long) == 4
     assert spg.step_kernel_name(_valid(spg, head_dim=48)) is None
     assert spg.step_launch_count(_valid(spg, head_dim=48)) == 0
+
+
+def test_dense_bypass_policy(spg):
+    """Quest's short-sequence rule: sparse pays only when the sequence has a
+    few times more pages than the budget selects (crossover measured at
+    about 2.5x on GB300)."""
+    p = _valid(spg, max_pages_per_seq=4096, num_phys_pages=8192, token_budget=16 * 128)
+    assert spg.spg_prefer_dense(p, 16 * 128)             # everything is selected anyway
+    assert spg.spg_prefer_dense(p, 16 * 320)             # 320 pages <= 2.5 x 128
+    assert not spg.spg_prefer_dense(p, 16 * 321)
+    assert not spg.spg_prefer_dense(p, 32768)
+    assert spg.spg_prefer_dense(p, 32768, ratio=20.0)    # a caller's own crossover
+    assert not spg.spg_prefer_dense(_valid(spg, selector="all", token_budget=0, n_sink_pages=0,
+                                           n_recent_pages=0), 16)
+    assert not spg.spg_prefer_dense(_valid(spg, head_dim=48), 16)
