@@ -342,6 +342,16 @@ spg_status spg_set_step_kernel(int32_t kernel);
 /* Waits for `stream`, then copies the workspace error word to *bits. */
 spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t stream);
 
+/* Test hook for the bounded waits.  Arms a one-shot flag in the workspace:
+ * the next split-K attention launch on it (sparse_decode_attention,
+ * dense_decode_attention, or a step that falls back to them) has its first
+ * CTA issue no copy for its first ring stage and never complete it, so the
+ * consumer's bounded wait (at most 100 ms) runs out with nothing in flight;
+ * the launch then finishes with SPG_DEVERR_TIMEOUT in the error word and
+ * its results are not valid (zero the workspace afterwards, as after any
+ * timeout).  For testing the error path only.  Asynchronous on `stream`. */
+spg_status spg_test_withhold_first_stage(void* ws, spg_stream_t stream);
+
 /* Clears the workspace error word (asynchronous on `stream`). */
 spg_status spg_clear_device_error(void* ws, spg_stream_t stream);
 

@@ -100,6 +100,7 @@ def _load():
         "spg_set_step_kernel": ([c_int32], c_int32),
         "spg_read_device_error": ([v, POINTER(c_int32), v], c_int32),
         "spg_clear_device_error": ([v, v], c_int32),
+        "spg_test_withhold_first_stage": ([v, v], c_int32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -270,3 +271,7 @@ def spg_read_device_error(ws, stream=None) -> int:
 
 def spg_clear_device_error(ws, stream=None):
     _check(LIB.spg_clear_device_error(_ptr(ws), _stream(stream)), "spg_clear_device_error")
+
+
+def spg_test_withhold_first_stage(ws, stream=None):
+    _check(LIB.spg_test_withhold_first_stage(_ptr(ws), _stream(stream)), "spg_test_withhold_first_stage")

@@ -28,7 +28,8 @@ int device_sm_count() {
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspace layout (every region 256-byte aligned):
-//   header    256 B: error word at 0, the scheduled step's queue counters at 64
+//   header    256 B: error word at 0, the scheduled step's queue counters at
+//             64, the bounded-wait test hook at 128
 //   counters  [B*Hkv] int32: split arrivals of the attention kernel
 //   sel_cnt.  [B*Hkv] int32: scoring CTAs done, for the fused selection
 //   scores    [B*Hkv][MP] fp32 (the scheduled step keeps its keys here)
@@ -61,6 +62,7 @@ Workspace carve_workspace(const spg_params& p, void* ws) {
   Workspace w{};
   w.err = reinterpret_cast<int32_t*>(base);
   w.sched_ctr = reinterpret_cast<int32_t*>(base + 64);
+  w.hook = reinterpret_cast<int32_t*>(base + 128);
   size_t off = 256;
   w.counters = reinterpret_cast<int32_t*>(base + off);
   off += align256(sizeof(int32_t) * B * Hkv);
@@ -432,6 +434,13 @@ spg_status spg_read_device_error(const void* ws, int32_t* bits, spg_stream_t str
   if (cudaMemcpy(bits, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return SPG_ECUDA;
   return SPG_OK;
+}
+
+spg_status spg_test_withhold_first_stage(void* ws, spg_stream_t stream) {
+  if (!ok_ptr(ws)) return SPG_EINVAL;
+  static const int32_t one = 1;
+  return cuda_status(cudaMemcpyAsync(static_cast<uint8_t*>(ws) + 128, &one, sizeof(one),
+                                     cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 spg_status spg_clear_device_error(void* ws, spg_stream_t stream) {

@@ -58,6 +58,7 @@ struct AttnArgs {
   float* pl;
   float* pacc;
   int32_t* counters;  // split arrivals per unit, zero between launches
+  int32_t* hook;      // test hook (workspace header): withhold the first stage of CTA (0, 0)
   float* out;
   float* lse;
   int32_t* err;
@@ -140,6 +141,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
     const T* vpool = static_cast<const T*>(a.v_pool);
     const uint64_t pol = policy_evict_first();
     bool ok = true;
+    // test hook (spg_test_withhold_first_stage): CTA (0, 0) issues no copy
+    // for its first stage and never completes it, so that the consumer's
+    // bounded wait runs out with nothing in flight; one shot
+    bool withhold = false;
+    if (a.hook && split == 0 && unit == 0) {
+      int hv = 0;
+      if (lane == 0) hv = atomicExch(a.hook, 0);
+      withhold = __shfl_sync(0xffffffffu, hv, 0) != 0;
+    }
     for (int base = 0; base < n_range && ok; base += 32) {
       int ph = -1, nv = 0;
       const int j = base + lane;
@@ -167,6 +177,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
         ok = __shfl_sync(0xffffffffu, lok ? 1 : 0, 0) != 0;
         if (!ok) break;
         const int np = min(PPS, nb - t0);
+        if (withhold && k == 0) continue;  // no copy, no arrival: the stage never completes
         if (lane >= t0 && lane < t0 + np) {
           const int i = lane - t0;
           uint8_t* dst = smem + static_cast<size_t>(stage) * sbytes + static_cast<size_t>(i) * pbytes;
@@ -403,6 +414,7 @@ cudaError_t launch_attention(const spg_params& p, const void* q, const void* k_p
   a.pl = ws.pl;
   a.pacc = ws.pacc;
   a.counters = ws.counters;
+  a.hook = ws.hook;
   a.err = ws.err;
   a.Hkv = p.num_kv_heads;
   a.S = p.page_size;

@@ -153,11 +153,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false when the barrier phase did not complete within
-// `limit` polls (the caller records SPG_DEVERR_TIMEOUT and stops issuing).
+// `limit` polls or 100 ms of wall time, whichever comes first (the caller
+// records SPG_DEVERR_TIMEOUT and stops issuing).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint32_t limit = (1u << 22)) {
-  for (uint32_t i = 0; i < limit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t i = 1; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 100ull * 1000 * 1000) return false;
+    }
+  }
   return false;
 }
 

@@ -13,6 +13,7 @@ namespace spg {
 // Workspace carved into its regions (all device pointers).
 struct Workspace {
   int32_t* err;     // error word (header)
+  int32_t* hook;    // test hook (header, byte 128): see spg_test_withhold_first_stage
   int32_t* counters;  // [B][Hkv] split arrivals of the attention kernel; zero between calls
   int32_t* sel_counters;  // [B][Hkv] scoring CTAs done, for the fused selection; zero between calls
   float* scores;    // [B][Hkv][MP]
