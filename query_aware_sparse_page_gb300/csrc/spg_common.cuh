@@ -140,28 +140,68 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// kCluster: acquire at cluster scope (the phase was completed by arrivals
+// from other CTAs of the cluster, see mbar_arrive_cluster)
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
   return ok != 0;
+}
+
+// arrive on the mbarrier at shared::cluster address `addr` (another CTA's),
+// release at cluster scope: what this thread did before (and what a CTA
+// barrier ordered before that) is visible to a cluster-scope wait that sees
+// the phase complete
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// arrive on the mbarrier at shared::cluster address `addr` (another CTA's)
+// and add `bytes` to its expected transaction count.  Relaxed: it orders
+// nothing before it (a release would first wait for this thread's earlier
+// global stores); the data it waits for come with st_async_u32.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(addr),
+               "r"(bytes)
+               : "memory");
+}
+
+// asynchronous 32-bit store into another CTA's shared memory: `addr` and the
+// mbarrier `bar` are shared::cluster addresses in that CTA; the store's
+// arrival completes 4 bytes of the barrier's transaction count
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(v), "r"(bar)
+               : "memory");
 }
 
 // Bounded wait: returns false when the barrier phase did not complete within
 // `limit` polls or 100 ms of wall time, whichever comes first (the caller
 // records SPG_DEVERR_TIMEOUT and stops issuing).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint32_t limit = (1u << 22)) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   uint64_t t0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
   for (uint32_t i = 1; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((i & 255u) == 0) {
       uint64_t t;
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

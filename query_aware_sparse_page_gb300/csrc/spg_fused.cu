@@ -25,7 +25,10 @@
 //  2. cluster barrier; the leader (rank 0) runs the exact top-k over the
 //     keys, adds the forced pages, writes sel / sel_cnt, and pushes each
 //     CTA's slice of the selection (physical page, valid tokens) into that
-//     CTA's shared memory; cluster barrier.
+//     CTA's shared memory with asynchronous stores (st.async) that complete
+//     the bytes of an mbarrier in the receiving CTA, plus one remote arrive
+//     carrying the byte count; each CTA starts attending as soon as its own
+//     slice has landed (no cluster barrier).
 //  3. attend: each consumer warp copies the K/V pages of its own ring stages
 //     (fp16/bf16, and int8 with d = 128 and an fp16 query: one 3-D TMA copy
 //     per page for K and for V, landing as 128-byte-swizzled tiles for the
@@ -33,16 +36,19 @@
 //     consumer; int8 scales by bulk copy) and refills a stage as soon as it
 //     has consumed it; the CTA's partial (m, l, acc) per query row goes into
 //     the leader's shared memory.
+//     The partials land where the leader kept its keys: a CTA writes them
+//     only after the leader's auxiliary warp has signalled, with a release
+//     at cluster scope made after the leader's last read of its keys.
 //  4. cluster barrier; the leader merges the partials and writes out / lse.
 // An auxiliary warp of the last CTA applies the metadata append of the new
 // token during the scan (Quest min/max of its page; the sketch of a block it
 // completes, split over every CTA's auxiliary warp): that page is forced, so
 // nothing in the step reads it.  The leader's auxiliary warp bulk-copies the
 // unit's page-table row into shared memory when it fits.
-// No CTA waits on another except at the three hardware cluster barriers,
-// which every thread of every CTA reaches on every path; all mbarrier waits
-// are bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still
-// reaches the cluster barriers.
+// CTAs wait on one another only at the two hardware cluster barriers, which
+// every thread of every CTA reaches on every path, and for the slice and the
+// keys-free signal the leader sends; all mbarrier waits are bounded (SPG_DEVERR_TIMEOUT) and a
+// CTA whose waits run out still reaches the cluster barriers.
 #include "spg_append.cuh"
 #include "spg_attn_core.cuh"
 #include "spg_internal.h"
@@ -197,6 +203,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   __shared__ int s_qc[4];
   __shared__ float s_sq;
   __shared__ __align__(8) uint64_t s_ptbar;  // leader: the page-table row has landed
+  __shared__ __align__(8) uint64_t s_slice;  // non-leader: its slice of the selection has landed
+  __shared__ __align__(8) uint64_t s_kfree;  // non-leader: the leader no longer reads its keys
   __shared__ int s_natt;  // pages of the selection this CTA attends to
   __shared__ float s_samax[kMaxCluster];  // sketch append: each CTA's |max|
   float sk_v[SEL ? kSketchVals : 1];       // sketch append: this lane's projected values
@@ -232,6 +240,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&s_ptbar, 1);
+    mbar_init(&s_slice, 1);
+    mbar_init(&s_kfree, 1);
     mbar_fence_init();
   }
   if constexpr (MMA) {
@@ -488,17 +498,43 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
           }
         }
         const uint32_t r = static_cast<uint32_t>(i / ppc), j = static_cast<uint32_t>(i - r * ppc);
-        st_cluster_u32(map_rank(s_att_ph + j, r), static_cast<uint32_t>(ph));
-        st_cluster_u32(map_rank(s_att_nv + j, r), static_cast<uint32_t>(nv));
+        if (r == 0) {
+          s_att_ph[j] = ph;
+          s_att_nv[j] = nv;
+        } else {
+          const uint32_t bar = map_rank(&s_slice, r);
+          st_async_u32(map_rank(s_att_ph + j, r), static_cast<uint32_t>(ph), bar);
+          st_async_u32(map_rank(s_att_nv + j, r), static_cast<uint32_t>(nv), bar);
+        }
       }
     }
     if (tid < C) {
       const int na = min(count, (tid + 1) * ppc) - min(count, tid * ppc);
-      st_cluster_u32(map_rank(&s_natt, static_cast<uint32_t>(tid)), static_cast<uint32_t>(na));
+      if (tid == 0) {
+        s_natt = na;
+      } else {
+        // the slice's bytes: na (ph, nv) pairs and na itself
+        const uint32_t r = static_cast<uint32_t>(tid), bar = map_rank(&s_slice, r);
+        st_async_u32(map_rank(&s_natt, r), static_cast<uint32_t>(na), bar);
+        mbar_arrive_expect_tx_cluster(bar, 4u * (2u * static_cast<uint32_t>(na) + 1u));
+      }
     }
     if (tid == 0) a.sel_cnt[unit] = count;
+    __syncthreads();  // the leader's own slice
+    // its keys are read no more: the other CTAs may write their partials
+    // there (the auxiliary warp, idle from here on, takes the release's wait)
+    if (warp == CW + 1 && lane > 0 && lane < C)
+      mbar_arrive_cluster(map_rank(&s_kfree, static_cast<uint32_t>(lane)));
+  } else {
+    // wait for this CTA's slice (bounded); without it the CTA attends to nothing
+    bool got = true;
+    if (threadIdx.x == 0) {
+      got = mbar_wait_bounded<true>(&s_slice, 0);
+      if (!got) record_error(a.err, SPG_DEVERR_TIMEOUT);
+    }
+    if (__syncthreads_and(got ? 1 : 0) == 0 && threadIdx.x == 0) s_natt = 0;
+    __syncthreads();
   }
-  cluster_sync();  // every CTA has its slice of the selection
 
   // ---------------------------------------------------------------- attend
   // Attend stage j holds pages [j * PPS, (j + 1) * PPS) of this CTA's slice;
@@ -602,7 +638,18 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   if (warp < CW) cons.store(s_m, s_l, s_acc, lane);
   __syncthreads();
   const uint32_t part_leader = map_rank(s_part, 0);
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+  bool kfree = true;
+  if (rank != 0) {
+    // the partials go where the leader's keys were: wait for its signal
+    // (long sent, normally); if that wait runs out the partial is not
+    // written (the error is recorded)
+    if (threadIdx.x == 0) {
+      kfree = mbar_wait_bounded<true>(&s_kfree, 0);
+      if (!kfree) record_error(a.err, SPG_DEVERR_TIMEOUT);
+    }
+    kfree = __syncthreads_and(kfree ? 1 : 0) != 0;
+  }
+  for (int idx = threadIdx.x; kfree && idx < G * D; idx += blockDim.x) {
     const int g = idx / D, c = idx % D;
     float M, Ls, A;
     lse_merge(s_m, s_l, s_acc, CW, G, D, g, c, M, Ls, A);
