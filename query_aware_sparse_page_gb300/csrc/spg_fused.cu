@@ -216,7 +216,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   uint64_t* empty = full + kMaxStages;
   int* s_np = reinterpret_cast<int*>(empty + kMaxStages);                // [stages] pages in stage
   int* s_nv = s_np + kMaxStages;                                          // [stages][8] valid tokens
-  float* s_rsc = reinterpret_cast<float*>(s_nv + kMaxStages * kMaxPagesPerStage);  // [stages][64]
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + a.keys_off);       // leader: keys
   float* s_part = reinterpret_cast<float*>(smem + a.keys_off);            // leader: partials
   int* s_sel = reinterpret_cast<int*>(smem + a.sel_off);                  // leader: selection
@@ -296,9 +295,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
         bulk_g2s(ring + static_cast<size_t>(stage) * sbytes, src0 + static_cast<size_t>(k) * R * rb,
                  nr * rb, &full[stage]);
       }
-      if constexpr (SEL == 1)
-        for (int r = lane; r < nr; r += 32)
-          s_rsc[stage * kMaxScanRows + r] = __ldg(a.sketch_scale + lrow0 + k * R + r);
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[stage]);
     }
@@ -401,19 +397,22 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       const int qc[4] = {s_qc[0], s_qc[1], s_qc[2], s_qc[3]};
       const int qbias = sketch_query_bias(qc);
       const float sq = s_sq;
+      const size_t lrow0 = static_cast<size_t>(unit) * a.MP + c0;
       for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
+        const int nr = min(R, rows - ks * R);
+        // the lane's block scale, loaded while the stage's codes land
+        const float bsc = lane < nr ? __ldg(a.sketch_scale + lrow0 + ks * R + lane) : 0.f;
         if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
           if (lane == 0) record_error(a.err, SPG_DEVERR_TIMEOUT);
           ok = false;
           break;
         }
-        const int nr = min(R, rows - ks * R);
         const uint8_t* st = ring + static_cast<size_t>(stage) * sbytes;
         // the stage's blocks (nr <= 32), one per lane; every scored block is
         // full (the open tail block is forced, never scored)
         if (lane < nr) {
-          const float cz = __fmul_rn(__fmul_rn(sq, s_rsc[stage * kMaxScanRows + lane]), a.inv_sqrt_d);
+          const float cz = __fmul_rn(__fmul_rn(sq, bsc), a.inv_sqrt_d);
           const float sc = sketch_block_score_lane(st + lane * rb, S, qc, qbias, cz);
           const uint32_t k0 = score_key(sc);
           st_cluster_u32(keys_leader + 4u * (c0 + ks * R + lane - lo), k0);
@@ -704,8 +703,7 @@ cudaError_t fused_typed(const spg_params& p, FusedArgs a, cudaStream_t st) {
   ring = max(ring, sizeof(float) * kConsumerWarps * G * (D + 2));
   ring = (ring + 127) & ~static_cast<size_t>(127);
   const size_t meta = sizeof(uint64_t) * 2 * kMaxStages +
-                      sizeof(int) * (kMaxStages + kMaxStages * kMaxPagesPerStage) +
-                      sizeof(float) * kMaxStages * kMaxScanRows;
+                      sizeof(int) * (kMaxStages + kMaxStages * kMaxPagesPerStage);
   const size_t keys_off = (ring + meta + 127) & ~static_cast<size_t>(127);
   const size_t keys_bytes =
       max(sizeof(uint32_t) * p.max_pages_per_seq, sizeof(float) * kMaxCluster * G * (D + 2));

@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(kThreads) k_sched(const __grid_constant__ Sche
           const int qbias = sketch_query_bias(qc);
           if (lane < nr) {
             const float cz = __fmul_rn(__fmul_rn(d.sq, f.rsc[slot][lane]), a.inv_sqrt_d);
-            const float sc = sketch_block_score_lane(stg + lane * rb, S, qc, qbias, cz);
+            const float sc = sketch_block_score_lane_t<0>(stg + lane * rb, S, qc, qbias, cz);
             kout[d.first + lane] = score_key(sc);
           }
         }

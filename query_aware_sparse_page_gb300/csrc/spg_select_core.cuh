@@ -841,27 +841,55 @@ __device__ __forceinline__ void sketch_block_scores4(const uint8_t* tile, int rb
 // at step t: the eight-byte reads of a half-warp then fall in different bank
 // pairs.  cz > 0 (a product of positive scales), so the maximum logit is cz
 // times the maximum integer dot, exactly; a second pass sums exp2 in the log2
-// domain.
+// domain.  SC: the block size as a compile-time constant (16, 32 or 64):
+// each token's integer dot is then computed once and kept in registers for
+// the second pass; 0: any S <= 128 (power of two), dots computed twice.
+template <int SC>
+__device__ __forceinline__ float sketch_block_score_lane_t(const uint8_t* blk, int S_, const int* qc,
+                                                           int bias, float cz) {
+  constexpr float kL2e = 1.4426950408889634f;
+  const int S = SC > 0 ? SC : S_;
+  const int rot = threadIdx.x & (S - 1);
+  if constexpr (SC > 0) {
+    int d[SC];
+    int dmax = INT_MIN;
+#pragma unroll
+    for (int t = 0; t < SC; ++t) {
+      const int tt = (t + rot) & (SC - 1);
+      const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
+      d[t] = sketch_token_dot(w, qc, bias);
+      dmax = max(dmax, d[t]);
+    }
+    const float zmax = static_cast<float>(dmax) * cz * kL2e;
+    float sum = 0.f;
+#pragma unroll
+    for (int t = 0; t < SC; ++t) sum += exp2f(static_cast<float>(d[t]) * cz * kL2e - zmax);
+    return (zmax + log2f(sum)) * kLn2;
+  } else {
+    int dmax = INT_MIN;
+    for (int t = 0; t < S; ++t) {
+      const int tt = (t + rot) & (S - 1);
+      const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
+      dmax = max(dmax, sketch_token_dot(w, qc, bias));
+    }
+    const float zmax = static_cast<float>(dmax) * cz * kL2e;
+    float sum = 0.f;
+    for (int t = 0; t < S; ++t) {
+      const int tt = (t + rot) & (S - 1);
+      const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
+      sum += exp2f(static_cast<float>(sketch_token_dot(w, qc, bias)) * cz * kL2e - zmax);
+    }
+    return (zmax + log2f(sum)) * kLn2;
+  }
+}
+
+// S: a power of two, 16 <= S <= 128 (warp-uniform)
 __device__ __forceinline__ float sketch_block_score_lane(const uint8_t* blk, int S, const int* qc,
                                                          int bias, float cz) {
-  constexpr float kL2e = 1.4426950408889634f;
-  const int rot = threadIdx.x & 31;
-  int dmax = INT_MIN;
-  for (int t = 0; t < S; ++t) {
-    int tt = t + rot;
-    if (tt >= S) tt -= S;
-    const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
-    dmax = max(dmax, sketch_token_dot(w, qc, bias));
-  }
-  const float zmax = static_cast<float>(dmax) * cz * kL2e;
-  float sum = 0.f;
-  for (int t = 0; t < S; ++t) {
-    int tt = t + rot;
-    if (tt >= S) tt -= S;
-    const uint2 w = *reinterpret_cast<const uint2*>(blk + tt * 8);
-    sum += exp2f(static_cast<float>(sketch_token_dot(w, qc, bias)) * cz * kL2e - zmax);
-  }
-  return (zmax + log2f(sum)) * kLn2;
+  if (S == 64) return sketch_block_score_lane_t<64>(blk, S, qc, bias, cz);
+  if (S == 32) return sketch_block_score_lane_t<32>(blk, S, qc, bias, cz);
+  if (S == 16) return sketch_block_score_lane_t<16>(blk, S, qc, bias, cz);
+  return sketch_block_score_lane_t<0>(blk, S, qc, bias, cz);
 }
 
 }  // namespace spg

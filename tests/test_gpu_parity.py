@@ -77,6 +77,13 @@ SMALL = {
                             kv_dtype="f16", q_dtype="f16"),
     "sals-s128-i8": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
                            page_size=128, seq_len=128 * 10 + 128, n_sel_pages=4),
+    # the sketch selector at 16- and 32-token blocks (a warp's lanes outnumber
+    # a block's tokens at 16)
+    "sals-s16-f16": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                           page_size=16, seq_len=16 * 90 + 5, n_sel_pages=12, kv_dtype="f16",
+                           q_dtype="f16"),
+    "sals-s32-i8": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                          page_size=32, seq_len=32 * 50 + 32, n_sel_pages=8),
     "quest-s32": scaled(get_workload("llama2-7b-mha-32k"), num_q_heads=4, num_kv_heads=2,
                         page_size=32, seq_len=32 * 150 + 7, n_sel_pages=20, needles_per_head=4),
     "quest-s64-bf16": scaled(get_workload("gqa-serving-b8-4k-64k"), batch=3, num_q_heads=8, num_kv_heads=2,
