@@ -7,8 +7,16 @@
 // Quest 完全拆解, 三段式 kernel (Approximate attention reads only the top-K
 // pages); Day 10·2 (softmax renormalised over the selected blocks only).
 //
-// Grid = (splits, batch * kv-heads), sized to one wave.  A CTA owns a
-// contiguous range of the unit's page list (selected ids, or every page for
+// Grid = (splits, batch * kv-heads), sized to one wave, for a selection (the
+// units' counts are alike).  The dense baseline plans its split by length
+// (SALS AICPU Tiling: the work of a ragged batch divided by a cost model of
+// each row's length): the grid is one wave of CTAs, and every CTA computes
+// the same plan from seq_lens, unit u taking parts(u) = ceil(w_u N / T)
+// consecutive CTAs (w_u its pages, T = sum of w_u, N = the CTAs less one per
+// unit, so that the rounding still fits the wave; 1 <= parts(u) <= the
+// split limit), then finds its own (unit, part) by a prefix over the units;
+// the parts of a unit cover its pages in equal contiguous ranges.  A CTA owns
+// a contiguous range of the unit's page list (selected ids, or every page for
 // the dense baseline) and is warp-specialised:
 //  * the producer warp resolves logical -> physical page ids 32 at a time
 //    (one lane per page) and streams each page's K and V tiles ([S][d] of one
@@ -58,6 +66,8 @@ struct AttnArgs {
   float* pl;
   float* pacc;
   int32_t* counters;  // split arrivals per unit, zero between launches
+  int planned;        // dense: (unit, part) from the length plan (grid = (CTAs, 1))
+  int units, plan_n;  // units; N of the plan (CTAs less one per unit)
   int32_t* hook;      // test hook (workspace header): withhold the first stage of CTA (0, 0)
   float* out;
   float* lse;
@@ -92,10 +102,66 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   int* s_np = reinterpret_cast<int*>(empty + kMaxStages);  // [stages] pages in stage
   int* s_nv = s_np + kMaxStages;                          // [stages][8] valid tokens
   __shared__ int s_last;
+  __shared__ int s_plan[3];  // unit, part, parts of the unit
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.y, split = blockIdx.x;
   const int Hkv = a.Hkv;
+  int unit = blockIdx.y, split = blockIdx.x, n_parts = gridDim.x;
+  int pages_per_split = a.pages_per_split;
+  if (a.planned) {
+    // the length plan (every CTA computes the same one) from seq_lens, which
+    // a previous kernel may have written
+    pdl_wait();
+    if (warp == 0) {
+      long long T = 0;
+      const int B = a.units / Hkv;
+      for (int bb = lane; bb < B; bb += 32) {
+        const int Lb = a.seq_lens[bb];
+        T += (Lb > 0 && Lb <= a.MP * a.S) ? (Lb + a.S - 1) / a.S : 0;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+      T *= Hkv;
+      int found_u = -1, found_j = 0, found_n = 1;
+      long long base = 0;
+      for (int u0 = 0; u0 < a.units; u0 += 32) {
+        const int u = u0 + lane;
+        int parts = 0;
+        if (u < a.units) {
+          const int Lb = a.seq_lens[u / Hkv];
+          const long long w = (Lb > 0 && Lb <= a.MP * a.S) ? (Lb + a.S - 1) / a.S : 0;
+          parts = T > 0 ? static_cast<int>((w * a.plan_n + T - 1) / T) : 1;
+          parts = max(1, min(kMaxSplits, parts));
+        }
+        int incl = parts;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const long long lo = base + incl - parts;
+        if (u < a.units && blockIdx.x >= lo && blockIdx.x < lo + parts) {
+          found_u = u;
+          found_j = static_cast<int>(blockIdx.x - lo);
+          found_n = parts;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, found_u >= 0);
+      if (lane == 0) s_plan[0] = -1;
+      __syncwarp();
+      if (found_u >= 0 && (hit & ((1u << lane) - 1u)) == 0) {
+        s_plan[0] = found_u;
+        s_plan[1] = found_j;
+        s_plan[2] = found_n;
+      }
+    }
+    __syncthreads();
+    if (s_plan[0] < 0) return;  // past the plan's last part: no work, nothing shared
+    unit = s_plan[0];
+    split = s_plan[1];
+    n_parts = s_plan[2];
+  }
   const int b = unit / Hkv, h = unit % Hkv;
   const int Hq = Hkv * G;
 
@@ -128,8 +194,14 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
       count = max(0, min(count, a.n_sel));
     }
   }
-  const int s0 = split * a.pages_per_split;
-  const int n_range = max(min(s0 + a.pages_per_split, count) - s0, 0);
+  int s0, n_range;
+  if (a.planned) {  // the part's share of the unit's pages
+    s0 = static_cast<int>(static_cast<long long>(split) * count / n_parts);
+    n_range = static_cast<int>(static_cast<long long>(split + 1) * count / n_parts) - s0;
+  } else {
+    s0 = split * pages_per_split;
+    n_range = max(min(s0 + pages_per_split, count) - s0, 0);
+  }
   const int n_st = (n_range + PPS - 1) / PPS;
   __syncthreads();
 
@@ -277,12 +349,12 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   __syncthreads();
   if (threadIdx.x == 0) {
     const int prev = atomicAdd(&a.counters[unit], 1);
-    s_last = (prev == static_cast<int>(gridDim.x) - 1);
+    s_last = (prev == n_parts - 1);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int n_split = gridDim.x;
+  const int n_split = n_parts;
   // weights of every split per row, in shared memory (reusing the ring)
   float* s_w = reinterpret_cast<float*>(smem);  // [G][n_split]
   float* s_M = s_w + G * kMaxSplits;            // [G]
@@ -371,13 +443,24 @@ cudaError_t attn_typed(const spg_params& p, const AttnArgs& a0, int pages_upper,
       per_sm < 1)
     per_sm = 1;
   const int slots = device_sm_count() * per_sm;
+  a.out = out;
+  a.lse = lse;
+  a.units = units;
+  if (!a.sel) {
+    // dense: the length plan over one wave (at least two CTAs per unit, so
+    // that N >= units); the sum of the parts is at most N + units CTAs
+    const int n_cta = max(slots, 2 * units);
+    a.planned = 1;
+    a.plan_n = n_cta - units;
+    a.pages_per_split = 0;
+    return launch_pdl(kern, dim3(n_cta, 1), dim3(threads), smem, st, a);
+  }
   int n_split = max(1, slots / units);
   n_split = min(n_split, min(kMaxSplits, max(pages_upper, 1)));
   const int pps_split = (max(pages_upper, 1) + n_split - 1) / n_split;
   n_split = max(1, (max(pages_upper, 1) + pps_split - 1) / pps_split);
   a.pages_per_split = pps_split;
-  a.out = out;
-  a.lse = lse;
+  a.planned = 0;
   return launch_pdl(kern, dim3(n_split, units), dim3(threads), smem, st, a);
 }
 
