@@ -136,6 +136,36 @@ __device__ __forceinline__ void sketch_project_row(const T* krow, float sc, cons
   }
 }
 
+// The projected values of one key row for the sketch outputs [u0, u0 + NU)
+// (u0 a multiple of 4), in the same order as sketch_project_row (each
+// product rounded, each output's sum in channel order): splitting the 16
+// outputs between lanes gives the same values.
+template <typename T, int D, int NU>
+__device__ __forceinline__ void sketch_project_row_part(const T* krow, float sc, const float* proj,
+                                                        int u0, float (&v)[NU]) {
+  constexpr int DS = 16;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) v[u] = 0.f;
+  const float4* P4 = reinterpret_cast<const float4*>(proj) + u0 / 4;  // [D][DS] row-major
+  for (int ic = 0; ic < D; ic += 16) {
+    float x[16];
+    load16_f32<T>(krow + ic, x);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float kv = x[e];
+      if constexpr (is_i8<T>()) kv = __fmul_rn(kv, sc);
+#pragma unroll
+      for (int q4 = 0; q4 < NU / 4; ++q4) {
+        const float4 pv = __ldg(P4 + (ic + e) * (DS / 4) + q4);
+        v[4 * q4] = __fadd_rn(v[4 * q4], __fmul_rn(kv, pv.x));
+        v[4 * q4 + 1] = __fadd_rn(v[4 * q4 + 1], __fmul_rn(kv, pv.y));
+        v[4 * q4 + 2] = __fadd_rn(v[4 * q4 + 2], __fmul_rn(kv, pv.z));
+        v[4 * q4 + 3] = __fadd_rn(v[4 * q4 + 3], __fmul_rn(kv, pv.w));
+      }
+    }
+  }
+}
+
 // Sketch of block blk of (b, h) by a whole CTA (blockDim.x >= S): thread t
 // projects token t, the block scale is absmax / 7 (1 for an all-zero
 // block), codes rint(v / scale) clamped to [-7, 7], two per byte, channel

@@ -116,21 +116,26 @@ __device__ __forceinline__ void smem_chunk(const uint8_t* p, uint32_t (&w)[CPL /
 
 // Sketch of the block completed by the token at L-1 (when L is a multiple of
 // S; SALS长序列推理优化, the low-rank index key of a block), split over the
-// auxiliary warps of the cluster's C CTAs: CTA r takes tokens
-// [r*S/C, (r+1)*S/C), one token per lane with all DS = 16 sketch dimensions.
-// Keys are dequantised (int8 code times its fp16 scale, exact in fp32) and
-// projected in fp32 with each product rounded and the sum taken in channel
-// order (no fused multiply-add).  Part 1 (during the scan) keeps the lane's
-// values in registers and sends the warp's |max| to every CTA; part 2 (after
-// the scan barrier) forms the block scale absmax / 7 and writes codes
-// rint(v / scale) clamped to [-7, 7], two per byte.  The block is the tail
-// block of this step (forced, never scored), so nothing in the step reads
-// what is written.
+// cluster's C CTAs: CTA r takes tokens [r*S/C, (r+1)*S/C), one token per
+// lane.  Its auxiliary warp computes all DS = 16 sketch dimensions, or, when
+// the CTA's scan fits its ring (the producer warp then has nothing left to
+// wait for), dimensions 0-7 while the producer warp computes 8-15.  Keys are
+// dequantised (int8 code times its fp16 scale, exact in fp32) and projected
+// in fp32 with each product rounded and each dimension's sum taken in
+// channel order (no fused multiply-add), so the split does not change a
+// value.  Part 1 (during the scan) keeps the lane's values in registers and
+// sends the CTA's |max| to every CTA; part 2 (after the scan barrier) forms
+// the block scale absmax / 7 and writes codes rint(v / scale) clamped to
+// [-7, 7], two per byte.  The block is the tail block of this step (forced,
+// never scored), so nothing in the step reads what is written.
 constexpr int kSketchVals = 16;  // one token's 16 sketch values per lane: S / C <= 32
 
+// half: 0 = the auxiliary warp, 1 = the producer warp (split only); every
+// lane of both warps calls it when split (they meet at named barrier 2)
 template <typename T, int D>
 __device__ void sketch_append_part1(const FusedArgs& a, int b, int h, int L, int lane, uint32_t rank,
-                                    int C, float (&v)[kSketchVals], float* s_samax) {
+                                    int C, int half, bool split, float (&v)[kSketchVals],
+                                    float* s_samax, float* s_hmax) {
   constexpr int DS = 16;
   const int S = a.S, blk = L / S - 1, tpc = S / C;
   const int t = static_cast<int>(rank) * tpc + lane;  // this lane's token
@@ -143,21 +148,40 @@ __device__ void sketch_append_part1(const FusedArgs& a, int b, int h, int L, int
       const size_t ph = static_cast<size_t>(phys) * a.Hkv + h;
       float sc = 1.f;
       if constexpr (is_i8<T>()) sc = __half2float(a.k_scale[ph * S + t]);
-      sketch_project_row<T, D>(static_cast<const T*>(a.k_pool) + (ph * S + t) * D, sc, a.proj, v);
+      const T* krow = static_cast<const T*>(a.k_pool) + (ph * S + t) * D;
+      if (split) {
+        float w[DS / 2];
+        sketch_project_row_part<T, D, DS / 2>(krow, sc, a.proj, half * (DS / 2), w);
 #pragma unroll
-      for (int u = 0; u < DS; ++u) amax = fmaxf(amax, fabsf(v[u]));
+        for (int u = 0; u < DS / 2; ++u) {
+          v[u] = w[u];
+          amax = fmaxf(amax, fabsf(w[u]));
+        }
+      } else {
+        sketch_project_row<T, D>(krow, sc, a.proj, v);
+#pragma unroll
+        for (int u = 0; u < DS; ++u) amax = fmaxf(amax, fabsf(v[u]));
+      }
     }
-  } else if (lane == 0 && rank == 0) {
+  } else if (lane == 0 && rank == 0 && half == 0) {
     record_error(a.err, SPG_DEVERR_PAGE_ID);
   }
   amax = warp_max(amax);
-  // every CTA's aux warp needs every CTA's |max| after the scan barrier
+  if (split) {
+    // the two warps' |max| (named barrier 2: the producer and auxiliary warps)
+    if (lane == 0) s_hmax[half] = amax;
+    asm volatile("bar.sync 2, 64;" ::: "memory");
+    amax = fmaxf(s_hmax[0], s_hmax[1]);
+    if (half != 0) return;
+  }
+  // every CTA needs every CTA's |max| after the scan barrier
   if (lane < C) st_cluster_f32(map_rank(s_samax + rank, static_cast<uint32_t>(lane)), amax);
 }
 
 template <typename T, int D>
 __device__ void sketch_append_part2(const FusedArgs& a, int b, int h, int L, int lane, uint32_t rank,
-                                    int C, const float (&v)[kSketchVals], const float* s_samax) {
+                                    int C, int half, bool split, const float (&v)[kSketchVals],
+                                    const float* s_samax) {
   constexpr int DS = 16;
   const int S = a.S, blk = L / S - 1, tpc = S / C;
   const int t = static_cast<int>(rank) * tpc + lane;
@@ -167,17 +191,26 @@ __device__ void sketch_append_part2(const FusedArgs& a, int b, int h, int L, int
   for (int r = 0; r < C; ++r) amax = fmaxf(amax, s_samax[r]);
   const float scale = amax > 0.f ? __fdiv_rn(amax, 7.0f) : 1.0f;
   const size_t lrow = (static_cast<size_t>(b) * a.Hkv + h) * a.MP + blk;
+  auto code2 = [&](float x0, float x1) {
+    const int c0 = max(-7, min(7, static_cast<int>(rintf(__fdiv_rn(x0, scale)))));
+    const int c1 = max(-7, min(7, static_cast<int>(rintf(__fdiv_rn(x1, scale)))));
+    return static_cast<uint32_t>((c0 & 0xf) | ((c1 & 0xf) << 4));
+  };
   if (lane < tpc) {
-    uint32_t w[2] = {0u, 0u};
+    uint8_t* dst = a.sketch_w + (lrow * S + t) * (DS / 2);
+    if (split) {  // this warp's half of the token's 8 bytes
+      uint32_t w = 0u;
 #pragma unroll
-    for (int k = 0; k < DS / 2; ++k) {
-      const int c0 = max(-7, min(7, static_cast<int>(rintf(__fdiv_rn(v[2 * k], scale)))));
-      const int c1 = max(-7, min(7, static_cast<int>(rintf(__fdiv_rn(v[2 * k + 1], scale)))));
-      w[k >> 2] |= static_cast<uint32_t>((c0 & 0xf) | ((c1 & 0xf) << 4)) << (8 * (k & 3));
+      for (int k = 0; k < DS / 4; ++k) w |= code2(v[2 * k], v[2 * k + 1]) << (8 * k);
+      *reinterpret_cast<uint32_t*>(dst + 4 * half) = w;
+    } else {
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int k = 0; k < DS / 2; ++k) w[k >> 2] |= code2(v[2 * k], v[2 * k + 1]) << (8 * (k & 3));
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
     }
-    *reinterpret_cast<uint2*>(a.sketch_w + (lrow * S + t) * (DS / 2)) = make_uint2(w[0], w[1]);
   }
-  if (rank == 0 && lane == 0) a.sketch_scale_w[lrow] = scale;
+  if (rank == 0 && lane == 0 && half == 0) a.sketch_scale_w[lrow] = scale;
 }
 
 template <typename T, typename TQ, int D, int G, int SEL>
@@ -207,6 +240,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   __shared__ __align__(8) uint64_t s_kfree;  // non-leader: the leader no longer reads its keys
   __shared__ int s_natt;  // pages of the selection this CTA attends to
   __shared__ float s_samax[kMaxCluster];  // sketch append: each CTA's |max|
+  __shared__ float s_hmax[2];             // sketch append: the two warps' |max| (split)
   float sk_v[SEL ? kSketchVals : 1];       // sketch append: this lane's projected values
 
   const int S = a.S, STAGES = a.stages, R = a.rows_per_stage, PPS = a.pages_per_stage;
@@ -264,6 +298,10 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   const int c0 = lo + min(nc, static_cast<int>(rank) * cpc);
   const int rows = lo + min(nc, static_cast<int>(rank + 1) * cpc) - c0;
   const int n_scan = (rows + R - 1) / R;
+  // the sketch append of a completed block: split between the auxiliary and
+  // producer warps when the producer issues every scan stage without waiting
+  const bool sk_append = SEL == 1 && a.append && L > 0 && L % S == 0;
+  const bool sk_split = sk_append && n_scan <= STAGES;
   const uint32_t keys_leader = map_rank(s_keys, 0);
   const uint32_t mm_leader = map_rank(s_mm, 0);
   bool ok = true;
@@ -298,6 +336,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[stage]);
     }
+    if constexpr (SEL == 1)  // the producer's half of the sketch append
+      if (sk_split)
+        sketch_append_part1<T, D>(a, b, h, L, lane, rank, C, 1, true, sk_v, s_samax, s_hmax);
   } else if (warp == CW + 1) {
     // auxiliary warp: the metadata append of the token at L-1.  Its page is
     // forced (n_recent >= 1), so neither this step's scan nor its attend
@@ -328,8 +369,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     } else {
       // the sketch of a block is written when the block fills (every CTA's
       // aux warp takes a slice)
-      if (a.append && L > 0 && L % S == 0)
-        sketch_append_part1<T, D>(a, b, h, L, lane, rank, C, sk_v, s_samax);
+      if (sk_append)
+        sketch_append_part1<T, D>(a, b, h, L, lane, rank, C, 0, sk_split, sk_v, s_samax, s_hmax);
     }
   } else {
     // consumers
@@ -433,8 +474,10 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
   cluster_sync();  // every key (and every warp's key min / max) is in the leader
 
   if constexpr (SEL == 1) {
-    if (warp == CW + 1 && a.append && L > 0 && L % S == 0)
-      sketch_append_part2<T, D>(a, b, h, L, lane, rank, C, sk_v, s_samax);
+    if (warp == CW + 1 && sk_append)
+      sketch_append_part2<T, D>(a, b, h, L, lane, rank, C, 0, sk_split, sk_v, s_samax);
+    else if (warp == CW && sk_split)
+      sketch_append_part2<T, D>(a, b, h, L, lane, rank, C, 1, true, sk_v, s_samax);
   }
 
   // ------------------------------------------------------------- selection
