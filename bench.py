@@ -43,9 +43,9 @@ NOMINAL_HBM_GBS = 8000.0
 # matches.
 NCU_TRAFFIC = {
     # workload: (DRAM bytes of one launch, code hash, kernel)
-    "llama2-7b-mha-32k": (67_790_848, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a", "k_fused"),
-    "long-scan-b4-128k": (205_888_768, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a", "k_fused"),
-    "sals-int8-b16-10k-4x": (100_546_816, "acfacd6946311deefe4311f12a5b916eebf88add8f86c077f441e2e3b70e174a", "k_fused"),
+    "llama2-7b-mha-32k": (67_940_608, "0056e603a241b1bbc13eb124f4294b787230c790f3b0c19211b7fb2a74c0586f", "k_fused"),
+    "long-scan-b4-128k": (205_374_464, "0056e603a241b1bbc13eb124f4294b787230c790f3b0c19211b7fb2a74c0586f", "k_fused"),
+    "sals-int8-b16-10k-4x": (100_837_376, "0056e603a241b1bbc13eb124f4294b787230c790f3b0c19211b7fb2a74c0586f", "k_fused"),
 }
 
 
@@ -317,14 +317,20 @@ def graph_runner(ops, names, R, K):
 
 
 def layer_bytes(w, layers):
-    """Algorithmic bytes of one step (layer 0's selection), and of the dense read."""
-    inp0, p0, b0 = layers[0]
-    sel_tok, cand, sel_pages = selection_stats(w, inp0, b0.sel, b0.sel_cnt)
-    meta_b, kv_b, small_b = step_bytes(w, None, sel_tok, cand, sel_pages)
-    lens = inp0.seq_lens.cpu().tolist()
+    """Algorithmic bytes of one step, and of the dense read, as the mean over
+    the layer replicas the timed regions cycle through (replicas of a ragged
+    batch draw different lengths; each replica's own selection is counted)."""
     kvb = 1 if w.kv_dtype == "i8" else 2
-    dense_b = sum(lens) * w.num_kv_heads * 2 * (w.head_dim * kvb + (2 if w.kv_dtype == "i8" else 0)) + small_b
-    return meta_b, kv_b, small_b, dense_b
+    tot = [0, 0, 0, 0]
+    for inp, _, bufs in layers:
+        sel_tok, cand, sel_pages = selection_stats(w, inp, bufs.sel, bufs.sel_cnt)
+        meta_b, kv_b, small_b = step_bytes(w, None, sel_tok, cand, sel_pages)
+        lens = inp.seq_lens.cpu().tolist()
+        dense_b = sum(lens) * w.num_kv_heads * 2 * (w.head_dim * kvb + (2 if w.kv_dtype == "i8" else 0)) + small_b
+        for i, x in enumerate((meta_b, kv_b, small_b, dense_b)):
+            tot[i] += x
+    n = len(layers)
+    return tuple(x // n for x in tot)
 
 
 def median_spread(xs):

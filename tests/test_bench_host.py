@@ -53,3 +53,32 @@ def test_traffic_is_reported_only_for_the_captured_code(bench, monkeypatch):
     monkeypatch.setattr(bench, "csrc_sha256", lambda d=None: "0" * 64)
     assert bench.ncu_traffic(wl) == (None, "kernel sources changed since the ncu capture")
     assert bench.ncu_traffic("no-such-workload")[0] is None
+
+
+def test_layer_bytes_average_the_replicas(bench):
+    """Replicas of a ragged batch draw different lengths: a timed step, which
+    cycles through them, is divided by the mean of their bytes, each replica
+    counted with its own selection."""
+    from types import SimpleNamespace
+
+    import torch
+
+    from synth import get_workload, make_inputs, scaled
+
+    w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=3, num_q_heads=8, num_kv_heads=2,
+               seq_range=(100, 3000), n_sel_pages=24)
+    layers = []
+    for l in range(2):
+        inp = make_inputs(w, device="cpu", seed_offset=l)
+        sel = torch.full((w.batch, w.num_kv_heads, w.n_sel_pages), -1, dtype=torch.int32)
+        cnt = torch.zeros((w.batch, w.num_kv_heads), dtype=torch.int32)
+        for b, L in enumerate(inp.seq_lens.tolist()):
+            n = min(-(-L // w.page_size), w.n_sel_pages)
+            sel[b, :, :n] = torch.arange(n, dtype=torch.int32)
+            cnt[b, :] = n
+        layers.append((inp, None, SimpleNamespace(sel=sel, sel_cnt=cnt)))
+    one = [bench.layer_bytes(w, [layer]) for layer in layers]
+    both = bench.layer_bytes(w, layers)
+    assert one[0] != one[1], "the two replicas should differ in length"
+    for i in range(4):
+        assert both[i] == (one[0][i] + one[1][i]) // 2
