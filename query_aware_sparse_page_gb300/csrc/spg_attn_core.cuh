@@ -441,7 +441,79 @@ struct AttnMmaI8 {
     l[0] = l[1] = 0.f;
   }
 
-  // one staged page with nv valid tokens (0 < nv <= S, S a multiple of 16)
+  // S^T of the 16 tokens at t0 (K codes at kb) against the query: the
+  // lane's logits sv (tokens t0 + g, t0 + g + 8; query columns 2t, 2t + 1),
+  // scaled by the tokens' K scales and the softmax scale, -inf past nv
+  __device__ __forceinline__ void qk16(uint32_t kb, const __half* ksc, int S, int nv, int t0,
+                                       int lane, float (&sv)[4]) const {
+    const int g = lane >> 2, mi = lane >> 3, r8 = lane & 7;
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    const int tok = t0 + (mi & 1) * 8 + r8;
+    const uint32_t rowb = kb + tok * D;
+#pragma unroll
+    for (int j = 0; j < NC; j += 2) {
+      const int chunk = j + (mi >> 1);
+      uint32_t r[4];
+      ldmatrix_x4(r, rowb + ((chunk ^ (tok & 7)) << 4));
+      // r[0]: tokens 0-7 of chunk j, r[1]: tokens 8-15, r[2], r[3]: chunk j + 1
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[4];
+        i8x4_to_h2(r[2 * h], a[0], a[2]);
+        i8x4_to_h2(r[2 * h + 1], a[1], a[3]);
+        if (h == 0)
+          mma_16816<__half>(c0, a, qb[j][0], qb[j][1]);
+        else
+          mma_16816<__half>(c1, a, qb[j + 1][0], qb[j + 1][1]);
+      }
+    }
+    const float ks0 = __half2float(ksc[min(t0 + g, S - 1)]);
+    const float ks1 = __half2float(ksc[min(t0 + g + 8, S - 1)]);
+    sv[0] = (c0[0] + c1[0]) * ks0 * scale;
+    sv[1] = (c0[1] + c1[1]) * ks0 * scale;
+    sv[2] = (c0[2] + c1[2]) * ks1 * scale;
+    sv[3] = (c0[3] + c1[3]) * ks1 * scale;
+    if (t0 + g >= nv) sv[0] = sv[1] = -INFINITY;
+    if (t0 + g + 8 >= nv) sv[2] = sv[3] = -INFINITY;
+  }
+
+  // O^T += V^T P^T for the 16 tokens at t0 (V codes at vb), p the lane's
+  // probabilities of those tokens (layout of qk16's sv)
+  __device__ __forceinline__ void pv16(uint32_t vb, const __half* vsc, int nv, int t0, int lane,
+                                       const float (&p)[4]) {
+    const int g = lane >> 2, r8 = lane & 7;
+    // p' = 256 p * V scale of the token (0 past the end)
+    const float vs0 = t0 + g < nv ? 256.f * __half2float(vsc[t0 + g]) : 0.f;
+    const float vs1 = t0 + g + 8 < nv ? 256.f * __half2float(vsc[t0 + g + 8]) : 0.f;
+    const float q0 = p[0] * vs0, q1 = p[1] * vs0, q2 = p[2] * vs1, q3 = p[3] * vs1;
+    const uint32_t h01 = pack2<__half>(q0, q1), h23 = pack2<__half>(q2, q3);
+    const float2 f01 = unpack2f<__half>(h01), f23 = unpack2f<__half>(h23);
+    const uint32_t l01 = pack2<__half>(q0 - f01.x, q1 - f01.y);
+    const uint32_t l23 = pack2<__half>(q2 - f23.x, q3 - f23.y);
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+    // matrices: tokens 0-7 / 8-15 of chunk j (lanes 0-15), then of chunk j + 1
+    const int tok = t0 + ((lane >> 3) & 1) * 8 + r8;
+    const uint32_t rowb = vb + tok * D;
+#pragma unroll
+    for (int j = 0; j < NC; j += 2) {
+      const int chunk = j + (lane >> 4);
+      uint32_t r[4];
+      ldmatrix_x4_trans(r, rowb + ((chunk ^ (tok & 7)) << 4));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[4];
+        i8x4t_to_h2(r[2 * h], a[0], a[1]);      // tokens 0-7: rows g (ch 2g), g + 8 (ch 2g + 1)
+        i8x4t_to_h2(r[2 * h + 1], a[2], a[3]);  // tokens 8-15
+        mma_16816<__half>(acc[j + h], a, bh0, bh1);
+        mma_16816<__half>(acc[j + h], a, bl0, bl1);
+      }
+    }
+  }
+
+  // one staged page with nv valid tokens (0 < nv <= S, S a multiple of 16),
+  // 32 tokens per step: the two 16-token products are independent, and one
+  // online-softmax update (max, rescale, exp) serves both
   __device__ void consume(uint8_t* st, int S, int nv, int lane) {
     const uint32_t kb = smem_u32(st);
     const uint32_t vb = kb + static_cast<uint32_t>(S) * D;
@@ -455,41 +527,13 @@ struct AttnMmaI8 {
         *reinterpret_cast<uint4*>(st + S * D + (nv + i / 8) * D + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
     }
-    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, r8 = lane & 7;
-    for (int t0 = 0; t0 < nv; t0 += 16) {
-      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int tok = t0 + (mi & 1) * 8 + r8;
-        const uint32_t rowb = kb + tok * D;
-#pragma unroll
-        for (int j = 0; j < NC; j += 2) {
-          const int chunk = j + (mi >> 1);
-          uint32_t r[4];
-          ldmatrix_x4(r, rowb + ((chunk ^ (tok & 7)) << 4));
-          // r[0]: tokens 0-7 of chunk j, r[1]: tokens 8-15, r[2], r[3]: chunk j + 1
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t a[4];
-            i8x4_to_h2(r[2 * h], a[0], a[2]);
-            i8x4_to_h2(r[2 * h + 1], a[1], a[3]);
-            if (h == 0)
-              mma_16816<__half>(c0, a, qb[j][0], qb[j][1]);
-            else
-              mma_16816<__half>(c1, a, qb[j + 1][0], qb[j + 1][1]);
-          }
-        }
-      }
-      const float ks0 = __half2float(ksc[min(t0 + g, S - 1)]);
-      const float ks1 = __half2float(ksc[min(t0 + g + 8, S - 1)]);
-      float sv[4];
-      sv[0] = (c0[0] + c1[0]) * ks0 * scale;
-      sv[1] = (c0[1] + c1[1]) * ks0 * scale;
-      sv[2] = (c0[2] + c1[2]) * ks1 * scale;
-      sv[3] = (c0[3] + c1[3]) * ks1 * scale;
-      const bool v0 = t0 + g < nv, v1 = t0 + g + 8 < nv;
-      if (!v0) sv[0] = sv[1] = -INFINITY;
-      if (!v1) sv[2] = sv[3] = -INFINITY;
-      float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+    for (int t0 = 0; t0 < nv; t0 += 32) {
+      const bool two = t0 + 16 < nv;  // the second 16 tokens hold a valid one
+      float sa[4], sb[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      qk16(kb, ksc, S, nv, t0, lane, sa);
+      if (two) qk16(kb, ksc, S, nv, t0 + 16, lane, sb);
+      float mx0 = fmaxf(fmaxf(sa[0], sa[2]), fmaxf(sb[0], sb[2]));
+      float mx1 = fmaxf(fmaxf(sa[1], sa[3]), fmaxf(sb[1], sb[3]));
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -515,39 +559,19 @@ struct AttnMmaI8 {
           acc[j][3] *= corr;
         }
       }
-      const float p0 = exp2f(sv[0] - m[0]), p1 = exp2f(sv[1] - m[1]);
-      const float p2 = exp2f(sv[2] - m[0]), p3 = exp2f(sv[3] - m[1]);
-      l[0] += p0 + p2;
-      l[1] += p1 + p3;
-      // p' = 256 p * V scale of the token (0 past the end)
-      const float vs0 = v0 ? 256.f * __half2float(vsc[t0 + g]) : 0.f;
-      const float vs1 = v1 ? 256.f * __half2float(vsc[t0 + g + 8]) : 0.f;
-      const float q0 = p0 * vs0, q1 = p1 * vs0, q2 = p2 * vs1, q3 = p3 * vs1;
-      const uint32_t h01 = pack2<__half>(q0, q1), h23 = pack2<__half>(q2, q3);
-      const float2 f01 = unpack2f<__half>(h01), f23 = unpack2f<__half>(h23);
-      const uint32_t l01 = pack2<__half>(q0 - f01.x, q1 - f01.y);
-      const uint32_t l23 = pack2<__half>(q2 - f23.x, q3 - f23.y);
-      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-      const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-      {
-        // matrices: tokens 0-7 / 8-15 of chunk j (lanes 0-15), then of chunk j + 1
-        const int tok = t0 + ((lane >> 3) & 1) * 8 + r8;
-        const uint32_t rowb = vb + tok * D;
-#pragma unroll
-        for (int j = 0; j < NC; j += 2) {
-          const int chunk = j + (lane >> 4);
-          uint32_t r[4];
-          ldmatrix_x4_trans(r, rowb + ((chunk ^ (tok & 7)) << 4));
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t a[4];
-            i8x4t_to_h2(r[2 * h], a[0], a[1]);      // tokens 0-7: rows g (ch 2g), g + 8 (ch 2g + 1)
-            i8x4t_to_h2(r[2 * h + 1], a[2], a[3]);  // tokens 8-15
-            mma_16816<__half>(acc[j + h], a, bh0, bh1);
-            mma_16816<__half>(acc[j + h], a, bl0, bl1);
-          }
-        }
-      }
+      float pa[4], pb[4];
+      pa[0] = exp2f(sa[0] - m[0]);
+      pa[1] = exp2f(sa[1] - m[1]);
+      pa[2] = exp2f(sa[2] - m[0]);
+      pa[3] = exp2f(sa[3] - m[1]);
+      pb[0] = exp2f(sb[0] - m[0]);
+      pb[1] = exp2f(sb[1] - m[1]);
+      pb[2] = exp2f(sb[2] - m[0]);
+      pb[3] = exp2f(sb[3] - m[1]);
+      l[0] += (pa[0] + pa[2]) + (pb[0] + pb[2]);
+      l[1] += (pa[1] + pa[3]) + (pb[1] + pb[3]);
+      pv16(vb, vsc, nv, t0, lane, pa);
+      if (two) pv16(vb, vsc, nv, t0 + 16, lane, pb);
     }
   }
 

@@ -196,6 +196,41 @@ def test_dense_baseline(name):
         assert np.abs(glse - res["lse"][(b, h)]).max() <= tol
 
 
+@pytest.mark.parametrize("case", ["skewed-with-empty", "all-empty", "one-unit-long"])
+def test_dense_length_plan_edges(case):
+    """The dense baseline's split planned by length: a unit with no pages, a
+    batch with no tokens at all, and one unit whose parts hit the split
+    limit (every other CTA of the wave has no work)."""
+    spg = _spg()
+    if case == "one-unit-long":
+        w = scaled(get_workload("tiny-quest-gqa4-1k"), seq_len=16 * 300 + 5, n_sel_pages=10)
+        lens = None
+    else:
+        w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=6, num_q_heads=8, num_kv_heads=2,
+                   seq_range=(1, 2), n_sel_pages=6)
+        lens = [0, 1, 16, 17, 95, 1600] if case == "skewed-with-empty" else [0] * 6
+    inp = make_inputs(w, device=DEV, seq_lens=lens)
+    p = spg.params_for(inp)
+    bufs = spg.alloc_buffers(p, DEV)
+    for _ in range(2):  # the arrival counters must return to zero for the next call
+        spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                                   inp.page_table, inp.seq_lens, bufs.out, bufs.lse, bufs.ws)
+    assert spg.spg_read_device_error(bufs.ws) == 0
+    oi = oracle_inputs(inp)
+    prm = oracle_params(w, selector="all")
+    res = decode.decode_step(oi, prm)
+    G = w.group
+    tol = TOL_OUT[w.kv_dtype]
+    for (b, h), out in res["out"].items():
+        gout = bufs.out[b, h * G : (h + 1) * G].cpu().numpy()
+        glse = bufs.lse[b, h * G : (h + 1) * G].cpu().numpy()
+        if int(inp.seq_lens[b]) == 0:
+            assert (gout == 0).all() and np.isneginf(glse).all()
+            continue
+        assert np.abs(gout - out).max() <= tol
+        assert np.abs(glse - res["lse"][(b, h)]).max() <= tol
+
+
 def test_full_budget_sparse_equals_dense():
     """Selecting every page reproduces dense attention (100% retention check)."""
     spg = _spg()
