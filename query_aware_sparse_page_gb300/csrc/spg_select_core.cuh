@@ -725,8 +725,13 @@ __device__ void sketch_index_query_warp(const TQ* qb, int G, int d, const float*
   }
   __syncwarp();
   float qt = 0.f;
-  if (lane < DS)
+  if (lane < DS) {
+    // one output per lane, its sum in channel order; unrolled so that the
+    // shared-memory loads run ahead of the chain of rounded adds (d is a
+    // multiple of 32)
+#pragma unroll 16
     for (int i = 0; i < d; ++i) qt = __fadd_rn(qt, __fmul_rn(s_qbar[i], s_P[i * DS + lane]));
+  }
   float am = fabsf(qt);
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
