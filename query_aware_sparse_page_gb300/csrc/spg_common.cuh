@@ -343,6 +343,17 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                    "memory");
 }
+// The same barrier split in two, for a cluster's first phase: every thread
+// arrives (relaxed) as soon as it starts, and waits before its first access
+// to another CTA's shared memory, so that every CTA of the cluster has
+// started by then.  Every thread of every CTA calls each once, in this order,
+// before its next cluster barrier.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 // shared::cluster address of `p` (a shared variable) in CTA `rank`
 __device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
   uint32_t r;

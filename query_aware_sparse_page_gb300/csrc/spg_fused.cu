@@ -283,6 +283,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       tma_prefetch_desc(&a.tmv);
     }
   }
+  // every CTA of the cluster must have started before another touches its
+  // shared memory: arrive now, wait before the first remote access below
+  cluster_arrive_relaxed();
   pdl_wait();
   int L = a.seq_lens[b];
   if (L < 0 || L > a.MP * S) {
@@ -336,6 +339,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[stage]);
     }
+    cluster_wait();
     if constexpr (SEL == 1)  // the producer's half of the sketch append
       if (sk_split)
         sketch_append_part1<T, D>(a, b, h, L, lane, rank, C, 1, true, sk_v, s_samax, s_hmax);
@@ -366,7 +370,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
                                    static_cast<T*>(a.minmax), a.err, a.Hkv, a.S, a.MP, a.n_phys, b, h,
                                    L, lane);
       }
-    } else {
+    }
+    cluster_wait();
+    if constexpr (SEL == 1) {
       // the sketch of a block is written when the block fills (every CTA's
       // aux warp takes a slice)
       if (sk_append)
@@ -378,6 +384,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
     if constexpr (SEL == 0) {
       QuestMma<TM, D, G> qm;
       qm.init(static_cast<const TM*>(a.q) + (static_cast<size_t>(b) * Hq + h * G) * D, lane);
+      cluster_wait();  // (the first stage is in flight meanwhile)
       for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
         if (!mbar_wait_bounded(&full[stage], (ks / STAGES) & 1)) {
@@ -438,6 +445,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32)
       const int qc[4] = {s_qc[0], s_qc[1], s_qc[2], s_qc[3]};
       const int qbias = sketch_query_bias(qc);
       const float sq = s_sq;
+      cluster_wait();
       const size_t lrow0 = static_cast<size_t>(unit) * a.MP + c0;
       for (int ks = warp; ks < n_scan; ks += CW) {
         const int stage = ks % STAGES;
