@@ -258,7 +258,7 @@ struct AttnMma {
       }
       __syncwarp();
     }
-    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    const int g = lane >> 2, mi = lane >> 3, r8 = lane & 7;
     for (int t0 = 0; t0 < nv; t0 += 16) {
       // S^T tile: two accumulation chains over the k-steps
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
