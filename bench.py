@@ -43,9 +43,9 @@ NOMINAL_HBM_GBS = 8000.0
 # matches.
 NCU_TRAFFIC = {
     # workload: (DRAM bytes of one launch, code hash, kernel)
-    "llama2-7b-mha-32k": (67_841_024, "ba7742fb55c62e46ee975f7035edc394047061fbfe50a9a0b7e4c95f924b16ba", "k_fused"),
-    "long-scan-b4-128k": (205_279_744, "ba7742fb55c62e46ee975f7035edc394047061fbfe50a9a0b7e4c95f924b16ba", "k_fused"),
-    "sals-int8-b16-10k-4x": (100_692_992, "ba7742fb55c62e46ee975f7035edc394047061fbfe50a9a0b7e4c95f924b16ba", "k_fused"),
+    "llama2-7b-mha-32k": (67_890_432, "ebd83aa240f926a217a97b62897c56d90e8d4000d7273d0df5caa2a35bec27ee", "k_fused"),
+    "long-scan-b4-128k": (205_280_000, "ebd83aa240f926a217a97b62897c56d90e8d4000d7273d0df5caa2a35bec27ee", "k_fused"),
+    "sals-int8-b16-10k-4x": (100_827_136, "ebd83aa240f926a217a97b62897c56d90e8d4000d7273d0df5caa2a35bec27ee", "k_fused"),
 }
 
 

@@ -35,6 +35,12 @@ CASES = {
                                num_kv_heads=2, seq_range=(100, 3000), n_sel_pages=48),
     "sketch": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
                      seq_len=64 * 30 + 17, n_sel_pages=20),
+    # Quest over an int8 pool: metadata in the query's type, tau the softmax
+    # scale; needles make a few pages hold most of the mass (without them
+    # the bounds are flat and p = 0.5 needs more pages than the budget)
+    "quest-i8": scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=8, num_kv_heads=2,
+                       page_size=16, seq_len=16 * 150 + 5, selector="quest", n_sel_pages=24,
+                       n_sink=1, n_recent=1, needles_per_head=4),
 }
 
 
