@@ -1,6 +1,6 @@
 // The whole decode step in one launch: metadata append (Quest), page scoring,
 // exact top-k, sparse flash-decoding and the log-sum-exp merge, with one
-// thread-block cluster of 8 CTAs per (batch, kv-head) unit.
+// thread-block cluster of up to 8 CTAs per (batch, kv-head) unit.
 //
 // Sources: Quest 完全拆解 (关键性估计算法: insert-time min/max, 核心机制: the
 // per-page bound, 三段式 kernel: estimate -> top-k -> approximate attention);
@@ -42,13 +42,18 @@
 //  4. cluster barrier; the leader merges the partials and writes out / lse.
 // An auxiliary warp of the last CTA applies the metadata append of the new
 // token during the scan (Quest min/max of its page; the sketch of a block it
-// completes, split over every CTA's auxiliary warp): that page is forced, so
-// nothing in the step reads it.  The leader's auxiliary warp bulk-copies the
-// unit's page-table row into shared memory when it fits.
-// CTAs wait on one another only at the two hardware cluster barriers, which
-// every thread of every CTA reaches on every path, and for the slice and the
-// keys-free signal the leader sends; all mbarrier waits are bounded (SPG_DEVERR_TIMEOUT) and a
-// CTA whose waits run out still reaches the cluster barriers.
+// completes, split over every CTA's auxiliary warp, and its producer warp
+// when that has nothing left to wait for): that page is forced, so nothing
+// in the step reads it.  The leader's auxiliary warp bulk-copies the unit's
+// page-table row into shared memory when it fits.
+// Every thread arrives (relaxed) on the cluster barrier as it starts and
+// waits before its warp's first access to another CTA's shared memory, so
+// every CTA has started before it is written to.  Beyond that, CTAs wait on
+// one another only at the cluster barriers after the scan and before the
+// merge, which every thread of every CTA reaches on every path, and for the
+// slice and the keys-free signal the leader sends; all mbarrier waits are
+// bounded (SPG_DEVERR_TIMEOUT) and a CTA whose waits run out still reaches
+// the cluster barriers.
 #include "spg_append.cuh"
 #include "spg_attn_core.cuh"
 #include "spg_internal.h"
