@@ -12,6 +12,7 @@ from oracle import decode, select
 from conftest import to_numpy
 
 TOL_OUT = {"f16": 2e-3, "bf16": 2e-3, "i8": 5e-3}  # max-abs on out and lse
+MASS_BAND = 1e-4  # |oracle cumulative mass - p| under which several top-p counts are correct
 REL_GAP = 1e-5  # k-th / (k+1)-th oracle score gap under which several selections are correct
 
 # Two GPU paths over the same selection differ only by arithmetic order, and
@@ -36,11 +37,13 @@ def assert_paths_agree(out_a, out_b, lse_a, lse_b, kv_dtype, vmax):
             assert bool((d <= tol).all()), f"lse differs by {d.max().item():.3e}"
 
 
-def run_step(inp, selector=None, n_sel_pages=None, fused=True, rebuild=True, bufs=None):
+def run_step(inp, selector=None, n_sel_pages=None, fused=True, rebuild=True, bufs=None,
+             top_p=0.0, min_pages=0):
     """Metadata rebuild, then select + attend on the GPU; returns host copies."""
     import query_aware_sparse_page_gb300 as spg
 
     p = spg.params_for(inp, selector=selector, n_sel_pages=n_sel_pages)
+    p.top_p, p.min_pages = top_p, min_pages
     if bufs is None:
         bufs = spg.alloc_buffers(p, inp.q.device)
     if rebuild:
@@ -110,6 +113,44 @@ def assert_selection_matches(gpu_sel, scores, P, n_sel, n_sink, n_recent, rel_ga
             f"selected page {p} scores {float(scores[p]):.6e}, below the tie band at {sk1 - band:.6e}")
 
 
+def allowed_top_p_counts(scores, ranked, k_budget, top_p, min_pages, tau):
+    """Candidate counts the adaptive budget may keep: the oracle's, and any
+    whose cumulative mass brackets p within MASS_BAND (then floored and
+    capped).  The GPU sums fp32 weights where the oracle sums fp64 ones, so
+    its count may differ only where the oracle's cumulative mass lies that
+    close to p."""
+    s = [float(scores[p]) for p in ranked]
+    mx = max(s)
+    w = [math.exp(tau * (x - mx)) for x in s]
+    z = math.fsum(w)
+    cum = np.cumsum(w) / z
+    ks = set()
+    for j in range(1, len(s) + 1):
+        lo = cum[j - 2] if j >= 2 else 0.0
+        if lo < top_p + MASS_BAND and cum[j - 1] >= top_p - MASS_BAND:
+            ks.add(j)
+    if not ks:
+        ks.add(len(s))
+    return {min(k_budget, max(k, min(min_pages, k_budget))) for k in ks}
+
+
+def top_p_count(gsel, scores, P, prm):
+    """Pages the adaptive budget kept (forced ones included), checked to be a
+    count the oracle's cumulative mass allows."""
+    forced = select.forced_pages(P, prm.n_sink, prm.n_recent)
+    fset = set(forced)
+    cand = [q for q in range(P) if q not in fset]
+    k_budget = min(max(prm.n_sel - len(forced), 0), len(cand))
+    k_gpu = len(gsel) - len(forced)
+    if k_budget > 0:
+        ranked = sorted(cand, key=lambda q: (-float(scores[q]), q))
+        ok = allowed_top_p_counts(scores, ranked, k_budget, prm.top_p, prm.min_pages, prm.tau)
+    else:
+        ok = {0}
+    assert k_gpu in ok, f"kept {k_gpu} candidates, allowed {sorted(ok)}"
+    return len(forced) + k_gpu
+
+
 def unit_inputs(inp, b, h):
     """Oracle inputs reduced to one (batch, kv-head) unit, pages renumbered 0..P-1."""
     w = inp.workload
@@ -145,7 +186,8 @@ def check_unit(inp, prm, bufs, b, h, tol):
             assert np.all(np.abs(gsc[cand] - ref) <= 1e-5 * (np.abs(ref) + 1.0)), \
                 f"score mismatch max {np.abs(gsc[cand] - ref).max():.3e}"
         assert np.all(np.isneginf(np.delete(gsc, cand)))
-        assert_selection_matches(gsel, scores, P, prm.n_sel, prm.n_sink, prm.n_recent)
+        n_sel = top_p_count(gsel, scores, P, prm) if prm.top_p > 0.0 else prm.n_sel
+        assert_selection_matches(gsel, scores, P, n_sel, prm.n_sink, prm.n_recent)
     out, lse = decode.attend_selection(sub, prm, 0, 0, gsel)
     gout = bufs.out[b, h * G : (h + 1) * G].cpu().numpy().astype(np.float64)
     glse = bufs.lse[b, h * G : (h + 1) * G].cpu().numpy().astype(np.float64)

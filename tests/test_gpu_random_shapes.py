@@ -4,11 +4,12 @@ Every draw picks a pool type (fp16, bf16, int8 with an fp16 or bf16 query),
 a selector (Quest, the sketch selector, or the probe selector on 16-bit
 pools), a head size, a query group, a page size whose K/V page fits the
 library's stage, a batch with lengths that include empty, one-token and
-page-aligned sequences, forced sink / recent pages and a budget, and a
-physical page order; the step then runs through the cluster kernel, the
+page-aligned sequences, forced sink / recent pages, a budget (trimmed, in
+half the draws, to the smallest prefix holding a fraction p of the score
+mass, with a floor), and a physical page order; the step then runs through the cluster kernel, the
 scheduled kernel and the separate score / select / attend entry points, and
 every unit's scores, selection and attention are checked against the oracle
-(the bars of the hand-picked parity shapes).
+(the bars of the hand-picked parity and top-p shapes).
 """
 
 import numpy as np
@@ -50,6 +51,9 @@ def _draw(seed):
         n_sink = int(rng.integers(0, 3))
         n_recent = int(rng.integers(1 if selector == "sketch" else 0, 3))
         n_sel = max(n_sink + n_recent + int(rng.integers(0, 40)), 1)
+        # half the draws trim the budget to a fraction of the score mass
+        top_p = float(rng.choice([0.5, 0.8, 0.95])) if rng.integers(0, 2) else 0.0
+        min_pages = int(rng.integers(0, 4))
         w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=B, num_q_heads=Hkv * G, num_kv_heads=Hkv,
                    head_dim=D, page_size=S, seq_len=max(max(lens), 1), seq_range=None, kv_dtype=kv,
                    q_dtype=q, selector=selector, n_sel_pages=n_sel, n_sink=n_sink, n_recent=n_recent,
@@ -60,16 +64,18 @@ def _draw(seed):
                             max_pages_per_seq=w.max_pages_per_seq, kv_dtype=kv, q_dtype=q,
                             selector=selector, token_budget=n_sel * S, n_sink_pages=n_sink,
                             n_recent_pages=n_recent)
+        p.top_p, p.min_pages = top_p, min_pages
         if spg.spg_validate(p) == 0:
-            return w, lens
+            return w, lens, top_p, min_pages
     raise AssertionError("no valid draw")
 
 
-def _run_probe(spg, inp, path):
+def _run_probe(spg, inp, path, top_p, min_pages):
     """The probe selector reads the key pool in place of page metadata."""
     import torch
 
     p = spg.params_for(inp)
+    p.top_p, p.min_pages = top_p, min_pages
     bufs = spg.alloc_buffers(p, DEV)
     pool = inp.k_pool
     spg.sparse_page_score(p, inp.q, inp.page_table, inp.seq_lens, pool, None, None, None,
@@ -103,11 +109,12 @@ def path(request):
 def test_random_shape_matches_oracle(seed, path):
     import query_aware_sparse_page_gb300 as spg
 
-    w, lens = _draw(seed)
+    w, lens, top_p, min_pages = _draw(seed)
     inp = make_inputs(w, device=DEV, seq_lens=lens)
     prm = oracle_params(w)
+    prm.top_p, prm.min_pages = top_p, min_pages
     if w.selector == "probe":
-        p, bufs, err = _run_probe(spg, inp, path)
+        p, bufs, err = _run_probe(spg, inp, path, top_p, min_pages)
         prm.n_probe = 8  # the library's default sample count
     else:
         p = spg.params_for(inp)
@@ -117,7 +124,7 @@ def test_random_shape_matches_oracle(seed, path):
             # select + attend still takes the chosen single-launch kernel
             want = "k_sched" if path == "sched" else "k_fused"
             assert spg.step_kernel_name(p) == want, spg.step_kernel_name(p)
-        p, bufs, err = run_step(inp, fused=path != "separate")
+        p, bufs, err = run_step(inp, fused=path != "separate", top_p=top_p, min_pages=min_pages)
     assert err == 0, f"device error {err:#x} ({w}, lengths {lens})"
     for b in range(w.batch):
         for h in range(w.num_kv_heads):

@@ -21,12 +21,12 @@ from oracle import decode, select as oselect
 from synth import get_workload, make_inputs, scaled
 
 from conftest import oracle_params
-from gpu_helpers import TOL_OUT, assert_selection_matches, gpu_selection, unit_inputs
+from gpu_helpers import (TOL_OUT, allowed_top_p_counts, assert_selection_matches, gpu_selection,
+                         unit_inputs)
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-MASS_BAND = 1e-4
 
 CASES = {
     "quest-mha": scaled(get_workload("llama2-7b-mha-32k"), num_q_heads=4, num_kv_heads=4,
@@ -42,24 +42,6 @@ CASES = {
                        page_size=16, seq_len=16 * 150 + 5, selector="quest", n_sel_pages=24,
                        n_sink=1, n_recent=1, needles_per_head=4),
 }
-
-
-def _allowed_counts(scores, ranked, k_budget, top_p, min_pages, tau):
-    """Candidate counts the GPU may keep: the oracle's, and any whose
-    cumulative mass brackets p within MASS_BAND (then floored and capped)."""
-    s = [float(scores[p]) for p in ranked]
-    mx = max(s)
-    w = [math.exp(tau * (x - mx)) for x in s]
-    z = math.fsum(w)
-    cum = np.cumsum(w) / z
-    ks = set()
-    for j in range(1, len(s) + 1):
-        lo = cum[j - 2] if j >= 2 else 0.0
-        if lo < top_p + MASS_BAND and cum[j - 1] >= top_p - MASS_BAND:
-            ks.add(j)
-    if not ks:
-        ks.add(len(s))
-    return {min(k_budget, max(k, min(min_pages, k_budget))) for k in ks}
 
 
 def _run(w, path, top_p, min_pages):
@@ -115,7 +97,7 @@ def test_adaptive_budget_matches_oracle(name, path, top_p, min_pages):
             k_gpu = len(gsel) - len(forced)
             if k_budget > 0:
                 ranked = sorted(cand, key=lambda q: (-float(scores[q]), q))
-                ok = _allowed_counts(scores, ranked, k_budget, top_p, min_pages, prm.tau)
+                ok = allowed_top_p_counts(scores, ranked, k_budget, top_p, min_pages, prm.tau)
                 assert k_gpu in ok, f"unit {(b, h)}: kept {k_gpu}, allowed {sorted(ok)}"
                 trimmed += k_gpu < k_budget
                 # the kept pages are the best k_gpu candidates (tie band as the fixed budget)
