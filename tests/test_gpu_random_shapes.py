@@ -8,7 +8,9 @@ page-aligned sequences, forced sink / recent pages, a budget (trimmed, in
 half the draws, to the smallest prefix holding a fraction p of the score
 mass, with a floor), and a physical page order; the step then runs through the cluster kernel, the
 scheduled kernel and the separate score / select / attend entry points, and
-every unit's scores, selection and attention are checked against the oracle
+through sparse_decode_step on both single-launch kernels from metadata one
+token old (the appended metadata must equal a rebuild bit for bit); every
+unit's scores, selection and attention are checked against the oracle
 (the bars of the hand-picked parity and top-p shapes).
 """
 
@@ -24,7 +26,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 N_CASES = 24
-PATHS = ["cluster", "sched", "separate"]
+PATHS = ["cluster", "sched", "separate", "step-cluster", "step-sched"]
 MAX_PAGE_BYTES = 34 * 1024  # K + V (+ int8 scales) of one page
 
 
@@ -94,12 +96,50 @@ def _run_probe(spg, inp, path, top_p, min_pages):
     return p, bufs, err
 
 
+def _run_decode_step(spg, inp, top_p, min_pages):
+    """sparse_decode_step: metadata as of one token earlier, then the step
+    appends the last token's metadata, selects and attends.  The appended
+    metadata must equal a full rebuild bit for bit; the scores are then taken
+    from it for the oracle comparison."""
+    import torch
+
+    p = spg.params_for(inp)
+    p.top_p, p.min_pages = top_p, min_pages
+    got = spg.alloc_buffers(p, DEV)
+    probe = inp.workload.selector == "probe"
+    proj = None if probe else inp.proj
+    if probe:
+        got.minmax = inp.k_pool  # the probe selector reads the pool itself
+    else:
+        ref = spg.alloc_buffers(p, DEV)
+        prev = (inp.seq_lens - 1).clamp(min=0)
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, prev, 1, got.minmax,
+                                    got.sketch, got.sketch_scale, proj, got.ws)
+        spg.sparse_page_meta_update(p, inp.k_pool, inp.k_scale, inp.page_table, inp.seq_lens, 1,
+                                    ref.minmax, ref.sketch, ref.sketch_scale, proj, ref.ws)
+    spg.sparse_decode_step(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                           inp.page_table, inp.seq_lens, got.minmax, got.sketch, got.sketch_scale,
+                           proj, got.sel, got.sel_cnt, got.out, got.lse, got.ws)
+    err = spg.spg_read_device_error(got.ws)
+    torch.cuda.synchronize()
+    if not probe and err == 0:
+        if got.sketch is None:
+            assert torch.equal(got.minmax, ref.minmax), "appended min/max differ from a rebuild"
+        else:
+            assert torch.equal(got.sketch, ref.sketch), "appended sketch codes differ from a rebuild"
+            assert torch.equal(got.sketch_scale, ref.sketch_scale), "appended sketch scales differ"
+    spg.sparse_page_score(p, inp.q, inp.page_table, inp.seq_lens, got.minmax, got.sketch,
+                          got.sketch_scale, proj, got.scores, got.ws)
+    torch.cuda.synchronize()
+    return p, got, err
+
+
 @pytest.fixture
 def path(request):
     import query_aware_sparse_page_gb300 as spg
 
     name = request.param
-    spg.spg_set_step_kernel(spg.STEP_KERNEL_SCHED if name == "sched" else spg.STEP_KERNEL_CLUSTER)
+    spg.spg_set_step_kernel(spg.STEP_KERNEL_SCHED if name.endswith("sched") else spg.STEP_KERNEL_CLUSTER)
     yield name
     spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
 
@@ -113,7 +153,14 @@ def test_random_shape_matches_oracle(seed, path):
     inp = make_inputs(w, device=DEV, seq_lens=lens)
     prm = oracle_params(w)
     prm.top_p, prm.min_pages = top_p, min_pages
-    if w.selector == "probe":
+    if path.startswith("step"):
+        if w.selector != "probe" and w.n_recent >= 1:
+            want = "k_sched" if path.endswith("sched") else "k_fused"
+            assert spg.step_kernel_name(spg.params_for(inp)) == want
+        p, bufs, err = _run_decode_step(spg, inp, top_p, min_pages)
+        if w.selector == "probe":
+            prm.n_probe = 8
+    elif w.selector == "probe":
         p, bufs, err = _run_probe(spg, inp, path, top_p, min_pages)
         prm.n_probe = 8  # the library's default sample count
     else:
