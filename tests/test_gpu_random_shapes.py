@@ -6,20 +6,24 @@ pools), a head size, a query group, a page size whose K/V page fits the
 library's stage, a batch with lengths that include empty, one-token and
 page-aligned sequences, forced sink / recent pages, a budget (trimmed, in
 half the draws, to the smallest prefix holding a fraction p of the score
-mass, with a floor), and a physical page order; the step then runs through the cluster kernel, the
-scheduled kernel and the separate score / select / attend entry points, and
-through sparse_decode_step on both single-launch kernels from metadata one
-token old (the appended metadata must equal a rebuild bit for bit); every
-unit's scores, selection and attention are checked against the oracle
-(the bars of the hand-picked parity and top-p shapes).
+mass, with a floor), and a physical page order.  The step then runs
+through the cluster kernel, the scheduled kernel and the separate score /
+select / attend entry points, and through sparse_decode_step on both
+single-launch kernels from metadata one token old (the appended metadata
+must equal a rebuild bit for bit); every unit's scores, selection and
+attention are checked against the oracle (the bars of the hand-picked
+parity and top-p shapes).  The dense baseline runs on the same draws
+against the oracle's attention over every page.
 """
 
 import numpy as np
 import pytest
 
+from oracle import decode
+
 from synth import get_workload, make_inputs, scaled
 
-from conftest import oracle_params
+from conftest import oracle_inputs, oracle_params
 from gpu_helpers import TOL_OUT, check_unit, run_step
 
 pytestmark = pytest.mark.gpu
@@ -176,3 +180,28 @@ def test_random_shape_matches_oracle(seed, path):
     for b in range(w.batch):
         for h in range(w.num_kv_heads):
             check_unit(inp, prm, bufs, b, h, TOL_OUT[w.kv_dtype])
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_shape_dense_matches_oracle(seed):
+    """The dense flash-decoding baseline (split planned by sequence length)
+    on the same draws: every unit's attention over its whole sequence."""
+    import query_aware_sparse_page_gb300 as spg
+
+    w, lens, _, _ = _draw(seed)
+    inp = make_inputs(w, device=DEV, seq_lens=lens)
+    p = spg.params_for(inp)
+    bufs = spg.alloc_buffers(p, DEV)
+    spg.dense_decode_attention(p, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
+                               inp.page_table, inp.seq_lens, bufs.out, bufs.lse, bufs.ws)
+    assert spg.spg_read_device_error(bufs.ws) == 0
+    res = decode.decode_step(oracle_inputs(inp), oracle_params(w, selector="all"))
+    G, tol = w.group, TOL_OUT[w.kv_dtype]
+    for (b, h), out in res["out"].items():
+        gout = bufs.out[b, h * G:(h + 1) * G].cpu().numpy().astype(np.float64)
+        glse = bufs.lse[b, h * G:(h + 1) * G].cpu().numpy().astype(np.float64)
+        assert np.abs(gout - out).max() <= tol, f"unit {(b, h)} out"
+        if lens[b] == 0:
+            assert np.isneginf(glse).all()
+        else:
+            assert np.abs(glse - res["lse"][(b, h)]).max() <= tol, f"unit {(b, h)} lse"
