@@ -238,9 +238,10 @@ spg_status sparse_decode_attention(const spg_params* p, const void* q, const voi
                                    const int32_t* sel, const int32_t* sel_cnt, float* out,
                                    float* lse, void* ws, size_t ws_bytes, spg_stream_t stream);
 
-/* sparse_page_select followed by sparse_decode_attention, one call; with page
- * tables of at most 8192 pages both run in a single cluster launch (see
- * sparse_decode_step). */
+/* sparse_page_select followed by sparse_decode_attention, one call; for the
+ * Quest and sketch selectors with page tables of at most 8192 pages both run
+ * in a single launch (see sparse_decode_step); the probe selector takes its
+ * selection launch and the attention launch. */
 spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const void* k_pool,
                                        const void* v_pool, const void* k_scale,
                                        const void* v_scale, const int32_t* page_table,
@@ -252,9 +253,10 @@ spg_status sparse_decode_select_attend(const spg_params* p, const void* q, const
 
 /* The whole decode step in one call: the metadata update for the token just
  * appended at seq_lens[b]-1 (as sparse_page_meta_update with rebuild == 0),
- * then sparse_decode_select_attend.  Where the parameters allow it (page
- * tables of at most 8192 pages), selection and attention run as one launch
- * of one 8-CTA thread-block cluster per (batch, kv-head), or as one
+ * then sparse_decode_select_attend.  Where the parameters allow it (Quest or
+ * sketch selector, page tables of at most 8192 pages), selection and
+ * attention run as one launch of one thread-block cluster of up to 8 CTAs per
+ * (batch, kv-head) (4 or 2 when the units would not fit one wave), or as one
  * persistent launch with task queues (spg_step_kernel says which); with
  * n_recent_pages >= 1 (and sketch_dim 16 for the sketch selector) the append
  * runs inside that launch too (the appended token's page is forced, so no
@@ -334,8 +336,8 @@ int32_t spg_step_launches(const spg_params* p);
 /* Process-wide preference between the two single-launch step kernels, for
  * comparing them: 0 = automatic (the cluster kernel where it applies, else
  * the scheduled kernel), 1 = the cluster kernel only, 2 = the scheduled
- * kernel only (shapes it does not take use the separate kernels).  Results are the
- * same up to the order of floating-point sums.  Not thread-safe with respect
+ * kernel only (shapes it does not take use the separate kernels).  Results
+ * are the same up to the order of floating-point sums.  Not thread-safe with respect
  * to launches in flight on other host threads.  SPG_EINVAL for other values. */
 spg_status spg_set_step_kernel(int32_t kernel);
 
