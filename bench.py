@@ -562,13 +562,17 @@ def run_e2e(args, spg, layers, stream, world, dev):
         rows = [(int(inp.page_table[bb, (L - 1) // S]), (L - 1) % S) for bb, L in enumerate(lens) if L > 0]
         phys = torch.tensor([r[0] for r in rows], dtype=torch.long, device=dev)
         slot = torch.tensor([r[1] for r in rows], dtype=torch.long, device=dev)
+        # row (page, head, slot) of a pool seen as [pages * Hkv * S][...]
+        Hkv = inp.workload.num_kv_heads
+        heads = torch.arange(Hkv, dtype=torch.long, device=dev)
+        rows_idx = ((phys[:, None] * Hkv + heads[None, :]) * S + slot[:, None]).reshape(-1)
         # what the host sends: q, then K, V (and their scales) of the new tokens
         parts = [inp.q]
         dsts = []
         for pool in (inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale):
             if pool is not None:
                 parts.append(pool[phys, :, slot].contiguous())
-                dsts.append(pool)
+                dsts.append(pool.view(-1, pool.shape[-1]) if pool.dim() == 4 else pool.view(-1))
         offs, n = [], 0
         for t in parts:
             offs.append(n)
@@ -580,19 +584,20 @@ def run_e2e(args, spg, layers, stream, world, dev):
         stage_d = torch.empty(n, dtype=torch.uint8, device=dev)
         views = [stage_d[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
                  for t, o in zip(parts, offs)]
+        srcs = [v.reshape(-1, v.shape[-1]) if v.dim() == 3 else v.reshape(-1) for v in views[1:]]
         n_out = b.out.numel()
         res_d = torch.empty(n_out + seg(b.lse.numel() * 4) // 4, dtype=torch.float32, device=dev)
         out_d = res_d[:n_out].view(b.out.shape)
         lse_d = res_d[n_out:n_out + b.lse.numel()].view(b.lse.shape)
         res_h = torch.empty(res_d.numel(), dtype=torch.float32).pin_memory()
-        plans.append((phys, slot, dsts, views, stage_h, stage_d, out_d, lse_d, res_d, res_h))
+        plans.append((rows_idx, srcs, dsts, views, stage_h, stage_d, out_d, lse_d, res_d, res_h))
 
     def e2e_step(i):
         inp, p, b = layers[i % R]
-        phys, slot, dsts, views, stage_h, stage_d, out_d, lse_d, res_d, res_h = plans[i % R]
+        rows_idx, srcs, dsts, views, stage_h, stage_d, out_d, lse_d, res_d, res_h = plans[i % R]
         stage_d.copy_(stage_h, non_blocking=True)
-        for pool, v in zip(dsts, views[1:]):
-            pool[phys, :, slot] = v
+        for dst, src in zip(dsts, srcs):
+            dst.index_copy_(0, rows_idx, src)
         spg.sparse_decode_step(p, views[0], inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale,
                                inp.page_table, inp.seq_lens, b.minmax, b.sketch, b.sketch_scale,
                                inp.proj, b.sel, b.sel_cnt, out_d, lse_d, b.ws)
