@@ -542,6 +542,14 @@ def run_ours(args, world, rank, local):
         print(json.dumps(res), flush=True)
 
 
+def pool_rows(phys, slot, n_kv_heads, page_size):
+    """Rows of (page phys[i], every kv-head, slot slot[i]) in a pool
+    [pages][Hkv][S][...] seen as [pages * Hkv * S][...], sequence-major then
+    head: the order of pool[phys, :, slot] flattened over its first two dims."""
+    heads = torch.arange(n_kv_heads, dtype=torch.long, device=phys.device)
+    return ((phys[:, None] * n_kv_heads + heads[None, :]) * page_size + slot[:, None]).reshape(-1)
+
+
 def run_e2e(args, spg, layers, stream, world, dev):
     """Same step through the public API with host buffers.  Every step one
     host -> device copy brings q and the appended token's K and V rows of
@@ -562,10 +570,7 @@ def run_e2e(args, spg, layers, stream, world, dev):
         rows = [(int(inp.page_table[bb, (L - 1) // S]), (L - 1) % S) for bb, L in enumerate(lens) if L > 0]
         phys = torch.tensor([r[0] for r in rows], dtype=torch.long, device=dev)
         slot = torch.tensor([r[1] for r in rows], dtype=torch.long, device=dev)
-        # row (page, head, slot) of a pool seen as [pages * Hkv * S][...]
-        Hkv = inp.workload.num_kv_heads
-        heads = torch.arange(Hkv, dtype=torch.long, device=dev)
-        rows_idx = ((phys[:, None] * Hkv + heads[None, :]) * S + slot[:, None]).reshape(-1)
+        rows_idx = pool_rows(phys, slot, inp.workload.num_kv_heads, S)
         # what the host sends: q, then K, V (and their scales) of the new tokens
         parts = [inp.q]
         dsts = []

@@ -82,3 +82,26 @@ def test_layer_bytes_average_the_replicas(bench):
     assert one[0] != one[1], "the two replicas should differ in length"
     for i in range(4):
         assert both[i] == (one[0][i] + one[1][i]) // 2
+
+
+def test_pool_rows_match_advanced_indexing():
+    """The end-to-end step writes the new tokens' K/V rows (and int8 scales)
+    through flat row indices: they must address exactly pool[phys, :, slot]."""
+    import torch
+
+    import bench
+
+    g = torch.Generator().manual_seed(3)
+    NP, Hkv, S, d = 41, 3, 16, 8
+    pool = torch.randn(NP, Hkv, S, d, generator=g)
+    scale = torch.randn(NP, Hkv, S, generator=g)
+    phys = torch.tensor([5, 40, 0, 17])
+    slot = torch.tensor([0, 15, 7, 3])
+    rows = bench.pool_rows(phys, slot, Hkv, S)
+    assert torch.equal(pool.view(-1, d)[rows], pool[phys, :, slot].reshape(-1, d))
+    assert torch.equal(scale.view(-1)[rows], scale[phys, :, slot].reshape(-1))
+    src = torch.randn(len(phys), Hkv, d, generator=g)
+    a, b = pool.clone(), pool.clone()
+    a.view(-1, d).index_copy_(0, rows, src.reshape(-1, d))
+    b[phys, :, slot] = src
+    assert torch.equal(a, b)
