@@ -167,6 +167,40 @@ def test_step_kernel_queries(spg):
     assert spg.step_launch_count(_valid(spg, head_dim=48)) == 0
 
 
+@pytest.mark.parametrize("selector", ["quest", "sketch", "probe"])
+@pytest.mark.parametrize("n_recent", [0, 1, 2])
+@pytest.mark.parametrize("pref", ["auto", "cluster", "sched"])
+def test_step_routing_grid(spg, selector, n_recent, pref):
+    """Host-only: the kernel sparse_decode_step takes and its launch count,
+    over selector x forced recent pages x step-kernel preference.  The probe
+    selector always takes its selection launch and the attention launch; the
+    others take the chosen single-launch kernel when the appended token's
+    page is forced (its append then runs inside the launch), else a separate
+    append, the scoring/selection launch and the attention launch; the
+    sketch selector requires a forced recent (tail) block."""
+    code = {"auto": spg.STEP_KERNEL_AUTO, "cluster": spg.STEP_KERNEL_CLUSTER,
+            "sched": spg.STEP_KERNEL_SCHED}[pref]
+    p = _valid(spg, selector=selector, n_recent_pages=n_recent, n_sink_pages=0,
+               page_size=64 if selector == "sketch" else 16)
+    if selector == "sketch" and n_recent == 0:
+        # the sketch selector always forces the open tail block
+        assert spg.spg_validate(p) != 0
+        assert spg.step_kernel_name(p) is None and spg.step_launch_count(p) == 0
+        return
+    assert spg.spg_validate(p) == 0
+    try:
+        spg.spg_set_step_kernel(code)
+        name, launches = spg.step_kernel_name(p), spg.step_launch_count(p)
+    finally:
+        spg.spg_set_step_kernel(spg.STEP_KERNEL_AUTO)
+    if selector == "probe":
+        assert (name, launches) == ("k_probe_select+k_attn", 2)
+    elif n_recent >= 1:
+        assert (name, launches) == ("k_sched" if pref == "sched" else "k_fused", 1)
+    else:
+        assert (name, launches) == (f"k_{selector}_select+k_attn", 3)
+
+
 def test_dense_bypass_policy(spg):
     """Quest's short-sequence rule: sparse pays only when the sequence has a
     few times more pages than the budget selects (crossover measured at
