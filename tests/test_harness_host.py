@@ -1,11 +1,12 @@
 """The GPU parity checker has teeth: host-only checks of gpu_helpers.check_unit.
 
 Buffers laid out as the library writes them are filled from the oracle
-itself, on the CPU; check_unit must accept them, and must reject each of a
-set of planted mistakes (a lower-scoring page swapped into the selection,
-an output element moved by more than the tolerance, a score off by more
-than the relative bar, a non-(-1) pad entry, an lse off, a top-p count
-that the oracle's cumulative mass does not allow).  No GPU is involved.
+itself, on the CPU, for the Quest, sketch and probe selectors; check_unit
+must accept them, and must reject each of a set of planted mistakes (a
+lower-scoring page swapped into the selection, an output element moved by
+more than the tolerance, a score off by more than the relative bar, a
+non-(-1) pad entry, an lse off, a top-p count that the oracle's cumulative
+mass does not allow).  No GPU is involved.
 """
 
 import types
@@ -52,13 +53,31 @@ def _fake_buffers(inp, prm):
     return bufs, scores
 
 
-@pytest.fixture(scope="module")
-def case():
-    w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=2, num_q_heads=4, num_kv_heads=2,
-               head_dim=64, seq_len=1200, seq_range=None, n_sel_pages=12, needles_per_head=2,
-               random_page_table=True)
-    inp = make_inputs(w, device="cpu", seq_lens=[1200, 150])  # 10 pages: two pad entries
+def _case_inputs(selector):
+    if selector == "sketch":
+        w = scaled(get_workload("sals-int8-b16-10k-4x"), batch=2, num_q_heads=4, num_kv_heads=2,
+                   seq_len=64 * 20, n_sel_pages=6)
+        lens = [64 * 20, 64 * 3 + 5]  # 4 blocks: two pad entries
+    else:
+        w = scaled(get_workload("gqa-serving-b8-4k-64k"), batch=2, num_q_heads=4, num_kv_heads=2,
+                   head_dim=64, seq_len=1200, seq_range=None, n_sel_pages=12, needles_per_head=2,
+                   random_page_table=True, selector=selector)
+        lens = [1200, 150]  # 10 pages: two pad entries
+    return w, make_inputs(w, device="cpu", seq_lens=lens)
+
+
+def _params(w, top_p=0.0):
     prm = oracle_params(w)
+    if w.selector == "probe":
+        prm.n_probe = 8
+    prm.top_p = top_p
+    return prm
+
+
+@pytest.fixture(scope="module", params=["quest", "sketch", "probe"])
+def case(request):
+    w, inp = _case_inputs(request.param)
+    prm = _params(w)
     bufs, scores = _fake_buffers(inp, prm)
     return w, inp, prm, bufs, scores
 
@@ -136,8 +155,7 @@ def test_top_p_count_outside_the_mass_band_is_caught(case):
     """With top-p on, the count kept must be one the oracle's cumulative mass
     allows: keeping the whole fixed budget where p = 0.5 trims is rejected."""
     w, inp, prm0, bufs_fixed, _ = case
-    prm = oracle_params(w)
-    prm.top_p, prm.min_pages = 0.5, 0
+    prm = _params(w, top_p=0.5)
     good, _ = _fake_buffers(inp, prm)
     _check_all(w, inp, prm, good)
     trimmed = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)
